@@ -1,0 +1,25 @@
+import functools
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
+    config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+
+
+@functools.lru_cache(maxsize=None)
+def cached_case(name, **kw):
+    from precision_flash_attention_attn_gb300.inputs import make_case
+    return make_case(name, **kw)
+
+
+def case(name, **kw):
+    """Seeded workload, generated once per test process."""
+    return cached_case(name, **kw)
