@@ -1,0 +1,162 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) flash-attention library (libfa.so).
+ *
+ * The operation is the attention forward and backward studied in "Why
+ * Low-Precision Transformer Training Fails: An Analysis on Flash Attention"
+ * (arXiv 2510.04212), in three numerical modes:
+ *
+ *   FA_MODE_BASELINE    safe softmax, section 3.4.4: Pbar = exp(S - rowmax S),
+ *                       Obar = Pbar V, O = Obar / rowsum(Pbar); O stored BF16.
+ *   FA_MODE_STABILISED  the stabilised safe softmax of section 3.4.5: with
+ *                       rm = rowmax(S) and rs = number of keys whose raw score
+ *                       equals rm exactly, the shift is beta*rm if rm > 0 and
+ *                       rs > 1, 0 if rm < 0 and rs > 1, rm otherwise (beta = 2,
+ *                       the value of the paper's Figure 7 runs); O stored BF16.
+ *                       The result equals the baseline's in exact arithmetic.
+ *   FA_MODE_FP32_OUT    as the baseline, but O is stored in FP32 (the
+ *                       "compute O in FP32 in the forward" isolation
+ *                       experiment of section 3.4.2, and the FP32 attention
+ *                       output practice described on the practices page).
+ *
+ * Shapes and layouts (all tensors contiguous, row-major):
+ *   q, k, v, dO, dq, dk, dv : BF16 [B, H, N, d]
+ *   o                       : BF16 [B, H, N, d] in modes 0 and 1,
+ *                             FP32 [B, H, N, d] in mode 2
+ *   lse                     : FP32 [B, H, N], natural log of
+ *                             sum_j exp(scale * q_i . k_j) over visible keys
+ *   S = scale * Q K^T with scale > 0; with causal = 1, key j is visible to
+ *   query i iff j <= i (queries and keys share the index range 0..N-1).
+ *   Supported: d in {64, 128}; 1 <= N <= 8388480; B*H*N*d < 2^31.
+ *
+ * Ownership: the caller allocates every buffer on the current CUDA device and
+ * keeps ownership; device pointers must be 16-byte aligned.  The library
+ * keeps no reference to any argument after a call returns.
+ *
+ * Asynchrony: every call only enqueues work on `stream` (NULL = the legacy
+ * default stream) and returns without synchronising.  Errors inside a kernel
+ * surface at the caller's next synchronisation, as for any CUDA launch;
+ * kernels also record bounded-wait timeouts in a device status word that
+ * fa_device_status() reads.
+ *
+ * Errors: every entry point returns an fa_status_t.  Arguments are checked
+ * before anything is enqueued; on a non-zero status nothing was launched.
+ * No entry point throws, aborts or exits.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_MODE_BASELINE = 0,
+    FA_MODE_STABILISED = 1,
+    FA_MODE_FP32_OUT = 2
+} fa_mode_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, causal/mode/scale out of range */
+    FA_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the current device is not sm_103 */
+    FA_ERR_ALLOC = 3,       /* a workspace allocation failed */
+    FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map) */
+    FA_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (fa_device_status) */
+} fa_status_t;
+
+/*
+ * fa_fwd -- attention forward (section 3.4.4 equations; section 3.4.5 shift in
+ * mode 1).  Reads q, k, v; writes o and lse.  Tiles: 128 queries x 128 keys;
+ * the online (tiled) softmax keeps per row the running max M, the running
+ * number C of keys equal to M, and the shift m = f(M, C) of the mode, and
+ * rescales the accumulator whenever m changes, so the final shift is the one
+ * the untiled rule gives.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, int causal, float scale, int mode,
+           fa_stream_t stream);
+
+/*
+ * fa_bwd -- attention backward from the saved LSE (P is recomputed as
+ * exp(S - LSE)); delta = rowsum(dO o O) uses the stored o of the same mode
+ * (BF16 in modes 0/1, FP32 in mode 2), dP = dO V^T, dS = scale * P o (dP -
+ * delta), dQ = dS K (sections 3.4.2-3.4.3), dK = dS^T Q, dV = P^T dO.
+ * Reads q, k, v, o, lse, dO; writes dq, dk, dv (BF16, FP32 accumulation).
+ * Allocates a stream-ordered workspace of B*H*N*d*4 + 2*B*H*ceil(N/128)*128*4
+ * bytes (cudaMallocAsync on `stream`, freed on `stream` before return);
+ * FA_ERR_ALLOC if that fails.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dO, void* dq, void* dk, void* dv,
+           int B, int H, int N, int d, int causal, float scale, int mode,
+           fa_stream_t stream);
+
+/*
+ * fa_tie_stats -- per-row diagnostics of the forward of `mode`:
+ *   tie_count[r] : number of visible keys whose FP32 raw score q.k equals the
+ *                  row maximum exactly (the rs of section 3.4.5 with eps = 0);
+ *   pv_err[r]    : sum over the d columns of (o[r,c] - O_ref[r,c]), the signed
+ *                  rounding error of the stored output, where O_ref is a
+ *                  CUDA-core FP32 recomputation of softmax(S) V (two passes,
+ *                  exact row max, compensated sums); o is the output of
+ *                  fa_fwd for the same mode (section 3.4.4, "Isolating the
+ *                  error to PV");
+ *   p_one        : nullable; p_one[r] = number of BF16 Pbar entries equal to
+ *                  1.0 fed to the PV product, p_one[B*H*N + r] = number of
+ *                  keys whose final weight (Pbar times later rescale factors)
+ *                  is exactly 1.0 (the condition of section 3.4.4, "Why
+ *                  P[T,t] = 1 is the critical condition").
+ * All three are [B, H, N] (p_one [2, B, H, N]); rows are r = (b*H + h)*N + i.
+ */
+int fa_tie_stats(const void* q, const void* k, const void* v, const void* o,
+                 int B, int H, int N, int d, int causal, float scale, int mode,
+                 int32_t* tie_count, float* pv_err, int32_t* p_one,
+                 fa_stream_t stream);
+
+/*
+ * fa_device_status -- synchronises `stream`, then returns FA_ERR_TIMEOUT if any
+ * kernel of this library on the current device recorded a bounded-wait
+ * timeout since the last reset, FA_ERR_CUDA if the synchronisation failed,
+ * else FA_OK.  reset != 0 clears the recorded status.
+ */
+int fa_device_status(fa_stream_t stream, int reset);
+
+/*
+ * Per-kernel timing (instrumentation for benchmarks).  Between
+ * fa_profile_start() and fa_profile_stop(), every kernel this library
+ * launches on the calling thread's current device is bracketed by a pair of
+ * CUDA events recorded on the launch stream.  fa_profile_stop() synchronises
+ * those events and, for each kernel kind k < n (see FA_KERNEL_*), writes the
+ * number of launches to launches[k] and their summed duration in
+ * milliseconds to total_ms[k] (either may be NULL).  Events are created
+ * lazily and reused; at most FA_PROFILE_MAX_LAUNCHES launches are recorded per
+ * session (later ones are counted in launches[] but not timed, and
+ * fa_profile_stop returns FA_ERR_ALLOC).  Not thread-safe across concurrent
+ * callers.
+ */
+enum {
+    FA_KERNEL_FWD = 0,       /* forward (modes 0-2) */
+    FA_KERNEL_FWD_STATS = 1, /* forward replay writing tie counts */
+    FA_KERNEL_BWD_PRE = 2,   /* delta, LSE*log2(e), dQ accumulator zeroing */
+    FA_KERNEL_BWD_MAIN = 3,  /* the five-MMA backward */
+    FA_KERNEL_DQ_CONVERT = 4,/* FP32 dQ accumulator -> BF16 */
+    FA_KERNEL_PV_ERR = 5,    /* CUDA-core reference for pv_err */
+    FA_KERNEL_COUNT = 6,
+    FA_PROFILE_MAX_LAUNCHES = 65536
+};
+int fa_profile_start(void);
+int fa_profile_stop(int n, int64_t* launches, double* total_ms);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

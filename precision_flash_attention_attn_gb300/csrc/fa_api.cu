@@ -1,0 +1,278 @@
+// C ABI of libfa (declared in include/fa.h): argument validation, device
+// checks, TMA tensor-map construction, workspace handling and dispatch to the
+// kernels.  No torch types, no exceptions across the boundary.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Device word where kernels record bounded-wait timeouts (one per device; the
+// host reaches it through its device address).
+__device__ int g_fa_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Current device: sm_103 check and the status word address.
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& di = g_dev[dev];
+    if (!di.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        di.supported = (major == 10 && minor == 3);
+        if (di.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+            di.status = static_cast<int*>(p);
+        }
+        di.probed = true;
+    }
+    if (!di.supported) return FA_ERR_UNSUPPORTED;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = &di;
+    return FA_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, int d, int causal, float scale, int mode) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 2) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    const long long total = static_cast<long long>(B) * H * N * (d > 0 ? d : 1);
+    if (total >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if (N > 65535 * fa::kBlockM) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+// 3-D view [BH][N][d] of a row-major tensor; box = inner x rows x 1,
+// 128-byte swizzle (inner * elem_bytes == 128).
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int BH, int N, int d,
+             int inner, int rows = fa::kBlockM) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                             static_cast<cuuint64_t>(d) * N * elem_bytes};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_ALLOC: return "FA_ERR_ALLOC";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, int mode, fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const int BH = B * H;
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+        return FA_ERR_CUDA;
+    fa::FwdArgs a{};
+    a.tm_q = &mq;
+    a.tm_k = &mk;
+    a.tm_v = &mv;
+    a.o = o;
+    a.lse = lse;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.causal = causal;
+    a.mode = mode;
+    a.scale = scale;
+    a.scale_log2 = log2e_times(scale);
+    a.status = di->status;
+    return fa::launch_fwd(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
+           fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const int BH = B * H;
+    const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
+    const size_t acc_bytes = static_cast<size_t>(BH) * N * d * sizeof(float);
+    const size_t row_bytes = static_cast<size_t>(BH) * Npad * sizeof(float);
+    const size_t ws_bytes = acc_bytes + 2 * row_bytes;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    void* ws = nullptr;
+    const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
+    if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    if (cudaMallocAsync(&ws, ws_bytes, st) != cudaSuccess || !ws) {
+        cudaGetLastError();
+        return FA_ERR_ALLOC;
+    }
+    float* dq_acc = static_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+    float* delta = lse2 + static_cast<size_t>(BH) * Npad;
+
+    CUtensorMap mq, mk, mv, mdo, macc;
+    rc = FA_OK;
+    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32))
+        rc = FA_ERR_CUDA;
+    if (rc == FA_OK) {
+        fa::BwdArgs a{};
+        a.tm_q = &mq;
+        a.tm_k = &mk;
+        a.tm_v = &mv;
+        a.tm_do = &mdo;
+        a.tm_dqacc = &macc;
+        a.o = o;
+        a.lse = lse;
+        a.dout = dO;
+        a.dq_acc = dq_acc;
+        a.lse2 = lse2;
+        a.delta = delta;
+        a.dq = dq;
+        a.dk = dk;
+        a.dv = dv;
+        a.BH = BH;
+        a.N = N;
+        a.Npad = Npad;
+        a.d = d;
+        a.causal = causal;
+        a.mode = mode;
+        a.scale = scale;
+        a.scale_log2 = log2e_times(scale);
+        a.status = di->status;
+        if (fa::launch_bwd(a, st) != cudaSuccess) rc = FA_ERR_CUDA;
+    }
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    return rc;
+}
+
+int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
+                 int causal, float scale, int mode, int32_t* tie_count, float* pv_err, int32_t* p_one,
+                 fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tie_count) ||
+        !aligned16(pv_err) || (p_one && !aligned16(p_one)))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const int BH = B * H;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap mq, mk, mv;
+    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+        return FA_ERR_CUDA;
+    fa::FwdArgs a{};
+    a.tm_q = &mq;
+    a.tm_k = &mk;
+    a.tm_v = &mv;
+    a.o = nullptr;
+    a.lse = nullptr;
+    a.tie_count = tie_count;
+    a.p_one = p_one;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.causal = causal;
+    a.mode = mode;
+    a.scale = scale;
+    a.scale_log2 = log2e_times(scale);
+    a.status = di->status;
+    if (fa::launch_fwd(a, true, st) != cudaSuccess) return FA_ERR_CUDA;
+    fa::StatsArgs s{};
+    s.q = q;
+    s.k = k;
+    s.v = v;
+    s.o = o;
+    s.pv_err = pv_err;
+    s.BH = BH;
+    s.N = N;
+    s.d = d;
+    s.causal = causal;
+    s.mode = mode;
+    s.scale = scale;
+    s.status = di->status;
+    return fa::launch_pv_err(s, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_device_status(fa_stream_t stream, int reset) {
+    DeviceInfo* di = nullptr;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (reset && h != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return h == 0 ? FA_OK : FA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,430 @@
+// Flash-attention forward for sm_103a: tiled online safe softmax in three
+// modes (baseline, stabilised, FP32 output), BF16 Q/K/V, FP32 TMEM
+// accumulators.
+//
+// Computes, per row i of a (batch, head):  S = Q K^T (raw scores),
+// Pbar = exp(alpha*S - m), Obar = Pbar V, O = Obar / rowsum(Pbar),
+// LSE = m + ln rowsum(Pbar)   ("Why Low-Precision Transformer Training Fails:
+// An Analysis on Flash Attention", section 3.4.4, safe-softmax equations).
+// The shift m is the running row max (modes 0, 2) or the stabilised shift of
+// section 3.4.5 (mode 1): with running max M and running count C of keys equal
+// to M, m = beta*M if M > 0 and C > 1, 0 if M < 0 and C > 1, else M (ties are
+// exact equality of FP32 raw scores, eps = 0).
+//
+// One CTA owns a 128-row query tile of one (batch, head) and streams 128-key
+// K/V tiles.  Warp roles:
+//   warps 0-3  softmax: thread t owns query row t (TMEM lane t).  Reads S from
+//              TMEM, masks, reduces row max and tie count, updates the shift,
+//              exponentiates (ex2), writes BF16 Pbar to swizzled shared
+//              memory, rescales the O accumulator in TMEM when the shift
+//              changes, and finally normalises and stores O and the LSE.
+//   warp 4     TMA producer: Q once, then K and V tiles through a ring.
+//   warp 5     MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers, then
+//              O += Pbar_j V_j into the TMEM O accumulator (tcgen05.mma,
+//              kind::f16, A and B from shared memory).
+// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256,256+d) O.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+template <int D, int MODE>
+struct FwdLayout {
+    static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows x D BF16
+    static constexpr int kStages = (D == 64) ? 3 : 2;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTileBytes;
+    static constexpr int kV = kK + kStages * kTileBytes;
+    static constexpr int kP = kV + kStages * kTileBytes;
+    static constexpr int kPBytes = kBlockM * kBlockN * 2;
+    // FP32-output mode feeds Pbar to the tensor core as hi + lo BF16 parts
+    static constexpr int kPLo = kP + kPBytes;
+    static constexpr int kBar = kPLo + (MODE == 2 ? kPBytes : 0);
+    // barriers
+    static constexpr int kQFull = 0;
+    static constexpr int kKFull = 1;
+    static constexpr int kVFull = kKFull + kStages;
+    static constexpr int kKVEmpty = kVFull + kStages;
+    static constexpr int kSFull = kKVEmpty + kStages;  // 2
+    static constexpr int kSEmpty = kSFull + 2;         // 2
+    static constexpr int kPFull = kSEmpty + 2;
+    static constexpr int kODone = kPFull + 1;
+    static constexpr int kDrain = kODone + 1;
+    static constexpr int kNumBars = kDrain + 1;
+    static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kBytes = kTmemSlot + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kOCol = 256;
+};
+
+struct FwdParams {
+    void* o;
+    float* lse;
+    int32_t* tie_count;
+    int32_t* p_one;
+    int BH, N;
+    float scale_log2;
+    int* status;
+};
+
+template <int D, int MODE, bool CAUSAL, bool STATS>
+__global__ void __launch_bounds__(192, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using L = FwdLayout<D, MODE>;
+    constexpr int S = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sb + L::kBar + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int qt = gridDim.y - 1 - blockIdx.y;  // longest causal tiles first
+    const int q0 = qt * kBlockM;
+    const int n_ktiles_all = (p.N + kBlockN - 1) / kBlockN;
+    const int n_kt = CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kQFull), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(L::kKFull + s), 1);
+            mbar_init(bar(L::kVFull + s), 1);
+            mbar_init(bar(L::kKVEmpty + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::kSFull + b), 1);
+            mbar_init(bar(L::kSEmpty + b), 128);
+        }
+        mbar_init(bar(L::kPFull), 128);
+        mbar_init(bar(L::kODone), 1);
+        mbar_init(bar(L::kDrain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+    if (warp == 4) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(bar(L::kQFull), L::kTileBytes);
+            for (int b = 0; b < D / 64; ++b)
+                tma_load_3d(sb + L::kQ + b * 16384, &tm_q, bar(L::kQFull), b * 64, q0, bh);
+            int issued = 0;
+            for (int j = 0; j < n_kt; ++j) {
+                const int s = j % S;
+                const uint32_t u = static_cast<uint32_t>(j / S);
+                if (j >= S && !mbar_wait(bar(L::kKVEmpty + s), (u - 1) & 1u, p.status)) break;
+                mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
+                                b * 64, j * kBlockN, bh);
+                mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTileBytes);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
+                                b * 64, j * kBlockN, bh);
+                issued = j + 1;
+            }
+            // Every copy this thread issued must have landed before the CTA
+            // may exit (normally long since true).
+            mbar_wait(bar(L::kQFull), 0, p.status);
+            for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j) {
+                const uint32_t u = static_cast<uint32_t>(j / S);
+                mbar_wait(bar(L::kKFull + j % S), u & 1u, p.status);
+                mbar_wait(bar(L::kVFull + j % S), u & 1u, p.status);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
+            constexpr uint32_t kIdPV = idesc_bf16(kBlockM, D, false, true);
+            bool ok = mbar_wait(bar(L::kQFull), 0, p.status);
+            auto issue_pv = [&](int t) {
+                const int s = t % S;
+                const uint32_t u = static_cast<uint32_t>(t / S);
+                ok = ok && mbar_wait(bar(L::kVFull + s), u & 1u, p.status);
+                ok = ok && mbar_wait(bar(L::kPFull), static_cast<uint32_t>(t) & 1u, p.status);
+                if (!ok) return;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint64_t a = sdesc_sw128(sb + L::kP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
+                    mma_bf16_ss(tmem + L::kOCol, a, b, kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (MODE == 2) {
+#pragma unroll
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(sb + L::kPLo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
+                        mma_bf16_ss(tmem + L::kOCol, a, b, kIdPV, 1u);
+                    }
+                }
+                mma_commit(bar(L::kODone));
+                mma_commit(bar(L::kKVEmpty + s));
+            };
+            for (int j = 0; j < n_kt && ok; ++j) {
+                const int s = j % S;
+                const uint32_t u = static_cast<uint32_t>(j / S);
+                const int buf = j & 1;
+                ok = mbar_wait(bar(L::kKFull + s), u & 1u, p.status);
+                if (ok && j >= 2)
+                    ok = mbar_wait(bar(L::kSEmpty + buf), static_cast<uint32_t>((j >> 1) - 1) & 1u, p.status);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(sb + L::kQ + koff, 16, 1024);
+                    const uint64_t b = sdesc_sw128(sb + L::kK + s * L::kTileBytes + koff, 16, 1024);
+                    mma_bf16_ss(tmem + buf * 128, a, b, kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(L::kSFull + buf));
+                if (j >= 1) issue_pv(j - 1);
+            }
+            if (ok) issue_pv(n_kt - 1);
+            // Drain: every MMA issued above has completed before TMEM is freed.
+            mma_commit(bar(L::kDrain));
+            mbar_wait(bar(L::kDrain), 0, p.status);
+        }
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int row = threadIdx.x;  // 0..127 == TMEM lane
+        const int qrow = q0 + row;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const float sl2 = p.scale_log2;
+        float M = -INFINITY;  // running max of raw scores
+        int C = 0;            // running count of keys equal to M
+        float m = -INFINITY;  // current shift, raw units
+        float mc = -INFINITY; // m * sl2
+        float l = 0.f;
+        int ones0 = 0, ones1 = 0;
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            const int buf = j & 1;
+            ok = mbar_wait(bar(L::kSFull + buf), static_cast<uint32_t>(j >> 1) & 1u, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBlockN];
+#pragma unroll
+            for (int c = 0; c < kBlockN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + buf * 128 + c * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(L::kSEmpty + buf));
+
+            const int k0 = j * kBlockN;
+            const bool need_mask = CAUSAL ? (k0 + kBlockN > q0) : (k0 + kBlockN > p.N);
+            if (need_mask) {
+                const int lim = CAUSAL ? (qrow - k0) : (p.N - 1 - k0);  // keep keys c <= lim
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c)
+                    if (c > lim) s[c] = -INFINITY;
+            }
+            float tm = s[0];
+#pragma unroll
+            for (int c = 1; c < kBlockN; ++c) tm = fmaxf(tm, s[c]);
+            if (MODE == 1 || STATS) {
+                int tc = 0;
+#pragma unroll
+                for (int c = 0; c < kBlockN; ++c) tc += (s[c] == tm) ? 1 : 0;
+                if (tm > M) {
+                    M = tm;
+                    C = tc;
+                } else if (tm == M) {
+                    C += tc;
+                }
+            } else {
+                M = fmaxf(M, tm);
+            }
+            float m_new = M;
+            if (MODE == 1 && C > 1) {
+                if (M > 0.f) m_new = kStabBeta * M;
+                else if (M < 0.f) m_new = 0.f;
+            }
+            const float mc_new = m_new * sl2;
+            const bool changed = (m_new != m);
+            const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
+            float lsum = 0.f;
+            uint32_t pk[kBlockN / 2];
+            uint32_t pl[kBlockN / 2];  // unused (and eliminated) unless MODE == 2
+#pragma unroll
+            for (int c = 0; c < kBlockN / 2; ++c) {
+                const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -mc_new));
+                const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -mc_new));
+                lsum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+                if (MODE == 2) {
+                    // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
+                    const float h0 = __uint_as_float(pk[c] << 16);
+                    const float h1 = __uint_as_float(pk[c] & 0xFFFF0000u);
+                    pl[c] = pack_bf16x2(p0 - h0, p1 - h1);
+                }
+            }
+            l = l * rsc + lsum;
+            m = m_new;
+            mc = mc_new;
+            if (STATS) {
+                int cnt = 0;
+#pragma unroll
+                for (int c = 0; c < kBlockN / 2; ++c)
+                    cnt += ((pk[c] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[c] >> 16) == 0x3F80u ? 1 : 0);
+                if (changed) ones1 = 0;
+                ones0 += cnt;
+                ones1 += cnt;
+            }
+            // Pbar_j may overwrite the shared P buffer and O may be rescaled
+            // only after O += Pbar_{j-1} V_{j-1} has completed.
+            if (j >= 1) {
+                ok = mbar_wait(bar(L::kODone), static_cast<uint32_t>(j - 1) & 1u, p.status);
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch)
+                st_shared_v4(sb + L::kP + (ch >> 3) * 16384 + sw128_off(row, ch & 7), pk[4 * ch],
+                             pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            if (MODE == 2) {
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch)
+                    st_shared_v4(sb + L::kPLo + (ch >> 3) * 16384 + sw128_off(row, ch & 7),
+                                 pl[4 * ch],
+                                 pl[4 * ch + 1],
+                                 pl[4 * ch + 2],
+                                 pl[4 * ch + 3]);
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, changed)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    const uint32_t ta = tmem + lane_off + L::kOCol + c * 32;
+                    tmem_ld32(ta, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
+                    tmem_st32(ta, r);
+                }
+                tmem_wait_st();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(L::kPFull));
+        }
+        if (ok) ok = mbar_wait(bar(L::kODone), static_cast<uint32_t>(n_kt - 1) & 1u, p.status);
+        const bool store = ok && qrow < p.N;
+        const size_t rowid = static_cast<size_t>(bh) * p.N + qrow;
+        if (STATS) {
+            if (store) {
+                p.tie_count[rowid] = C;
+                if (p.p_one) {
+                    p.p_one[rowid] = ones0;
+                    p.p_one[static_cast<size_t>(p.BH) * p.N + rowid] = ones1;
+                }
+            }
+        } else if (__all_sync(0xffffffffu, ok)) {
+            // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + L::kOCol + c * 32, r);
+                tmem_wait_ld();
+                if (!store) continue;
+                if (MODE == 2) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + rowid * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
+                                             __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + rowid * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
+                        dst[e] = w;
+                    }
+                }
+            }
+            // LSE = m*alpha + ln(l), natural log of the scaled-score normaliser
+            if (store) p.lse[rowid] = (mc + lg2_approx(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int D, int MODE, bool CAUSAL, bool STATS>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+    using L = FwdLayout<D, MODE>;
+    auto kern = fwd_kernel<D, MODE, CAUSAL, STATS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    FwdParams p;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.tie_count = a.tie_count;
+    p.p_one = a.p_one;
+    p.BH = a.BH;
+    p.N = a.N;
+    p.scale_log2 = a.scale_log2;
+    p.status = a.status;
+    const int n_qt = (a.N + kBlockM - 1) / kBlockM;
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_qt));
+    prof_begin(STATS ? 1 : 0, stream);
+    kern<<<grid, 192, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    prof_end(STATS ? 1 : 0, stream);
+    return cudaGetLastError();
+}
+
+template <int D, int MODE>
+cudaError_t dispatch_causal(const FwdArgs& a, bool stats, cudaStream_t st) {
+    if (a.causal) return stats ? launch_fwd_t<D, MODE, true, true>(a, st) : launch_fwd_t<D, MODE, true, false>(a, st);
+    return stats ? launch_fwd_t<D, MODE, false, true>(a, st) : launch_fwd_t<D, MODE, false, false>(a, st);
+}
+
+template <int D>
+cudaError_t dispatch_mode(const FwdArgs& a, bool stats, cudaStream_t st) {
+    switch (a.mode) {
+        case 0: return dispatch_causal<D, 0>(a, stats, st);
+        case 1: return dispatch_causal<D, 1>(a, stats, st);
+        default: return dispatch_causal<D, 2>(a, stats, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, bool stats, cudaStream_t stream) {
+    return a.d == 64 ? dispatch_mode<64>(a, stats, stream) : dispatch_mode<128>(a, stats, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,69 @@
+// Internal launch interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kBlockM = 128;  // query rows per tile (one TMEM lane per row)
+constexpr int kBlockN = 128;  // keys per tile
+
+// Stabilised-softmax constant beta (the paper's Figure 7 runs use beta = 2).
+constexpr float kStabBeta = 2.0f;
+
+struct FwdArgs {
+    const CUtensorMap* tm_q;
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    void* o;            // [BH, N, d] BF16 (modes 0, 1) or FP32 (mode 2); null: not written
+    float* lse;         // [BH, N]; null: not written
+    int32_t* tie_count; // statistics variant only: [BH, N]
+    int32_t* p_one;     // statistics variant only, nullable: [2][BH, N]
+    int BH, N, d, causal, mode;
+    float scale;        // alpha
+    float scale_log2;   // alpha * log2(e)
+    int* status;        // device status word
+};
+
+struct BwdArgs {
+    const CUtensorMap* tm_q;
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    const CUtensorMap* tm_do;
+    const CUtensorMap* tm_dqacc;  // FP32 [BH, N, d] accumulator (reduce-add target)
+    const void* o;                // [BH, N, d] BF16 or FP32 (mode 2)
+    const float* lse;             // [BH, N]
+    const void* dout;             // [BH, N, d] BF16
+    float* dq_acc;                // FP32 [BH, N, d] workspace
+    float* lse2;                  // FP32 [BH, Npad] workspace: LSE * log2(e)
+    float* delta;                 // FP32 [BH, Npad] workspace: rowsum(dO o O)
+    void* dq;                     // [BH, N, d] BF16
+    void* dk;
+    void* dv;
+    int BH, N, Npad, d, causal, mode;
+    float scale, scale_log2;
+    int* status;
+};
+
+struct StatsArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;     // BF16 or FP32 (mode 2)
+    float* pv_err;     // [BH, N]
+    int BH, N, d, causal, mode;
+    float scale;
+    int* status;
+};
+
+// Kernel timing hooks (no-ops unless a profiling session is active).
+void prof_begin(int kind, cudaStream_t stream);
+void prof_end(int kind, cudaStream_t stream);
+
+cudaError_t launch_fwd(const FwdArgs& a, bool stats, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_pv_err(const StatsArgs& a, cudaStream_t stream);
+
+}  // namespace fa

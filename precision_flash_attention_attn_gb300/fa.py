@@ -1,0 +1,168 @@
+"""Thin Python binding of libfa (include/fa.h): argument marshalling only.
+
+The names mirror the C ABI: ``fa_fwd``, ``fa_bwd``, ``fa_tie_stats``,
+``fa_device_status`` and ``fa_status_string``.  Tensor arguments are torch
+CUDA tensors (their data pointers are passed through) or raw integer device
+addresses; every step of the computation runs in the library's kernels.  A
+non-zero status raises :class:`FAError`.  ``attention_fwd`` / ``attention_bwd``
+/ ``tie_stats`` additionally allocate the outputs with torch.
+
+If the shared library has not been built this module raises on import: there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from .build import INCLUDE, LIB
+
+MODES = {"baseline": 0, "stabilised": 1, "fp32_out": 2}
+FA_OK = 0
+
+if not os.path.exists(LIB):
+    raise ImportError(f"libfa.so is not built ({LIB}); run __graft_entry__.build() first")
+
+_lib = ctypes.CDLL(LIB)
+_P = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+
+_lib.fa_fwd.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
+_lib.fa_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
+_lib.fa_tie_stats.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P, _P, _P, _P]
+_lib.fa_device_status.argtypes = [_P, _i]
+_lib.fa_profile_start.argtypes = []
+_lib.fa_profile_stop.argtypes = [_i, _P, _P]
+_lib.fa_status_string.argtypes = [_i]
+_lib.fa_status_string.restype = ctypes.c_char_p
+for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
+            _lib.fa_profile_stop):
+    _fn.restype = ctypes.c_int
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} returned {status} ({fa_status_string(status)})")
+        self.status = status
+
+
+def library_path() -> str:
+    return LIB
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/fa.h."""
+    with open(os.path.join(INCLUDE, "fa.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != FA_OK:
+        raise FAError(fn, rc)
+    return rc
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.fa_status_string(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, mode, stream=None, check=True):
+    rc = _lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(causal),
+                     float(scale), int(mode), _stream(stream))
+    return _check("fa_fwd", rc) if check else rc
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream=None, check=True):
+    rc = _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                     _ptr(dv), B, H, N, d, int(causal), float(scale), int(mode), _stream(stream))
+    return _check("fa_bwd", rc) if check else rc
+
+
+def fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err, p_one=None,
+                 stream=None, check=True):
+    rc = _lib.fa_tie_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, d, int(causal), float(scale),
+                           int(mode), _ptr(tie_count), _ptr(pv_err), _ptr(p_one), _stream(stream))
+    return _check("fa_tie_stats", rc) if check else rc
+
+
+def fa_device_status(stream=None, reset=True) -> int:
+    return int(_lib.fa_device_status(_stream(stream), int(reset)))
+
+
+KERNELS = ["fwd", "fwd_stats", "bwd_pre", "bwd_main", "dq_convert", "pv_err"]
+
+
+def fa_profile_start() -> None:
+    _check("fa_profile_start", _lib.fa_profile_start())
+
+
+def fa_profile_stop() -> dict:
+    """{kernel: (launches, total_ms)} for the session just ended."""
+    n = len(KERNELS)
+    launches = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    _check("fa_profile_stop", _lib.fa_profile_stop(n, launches, ms))
+    return {k: (int(launches[i]), float(ms[i])) for i, k in enumerate(KERNELS)}
+
+
+# --------------------------------------------------------------------------
+# Allocating conveniences (torch tensors in, torch tensors out)
+# --------------------------------------------------------------------------
+
+def _shape(q):
+    B, H, N, d = q.shape
+    return B, H, N, d
+
+
+def attention_fwd(q, k, v, causal=True, scale=None, mode=0, stream=None):
+    """Returns (o, lse).  o is BF16, or FP32 in mode 2."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty((B, H, N, d), device=q.device,
+                    dtype=torch.float32 if mode == 2 else torch.bfloat16)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, mode, stream)
+    return o, lse
+
+
+def attention_bwd(q, k, v, o, lse, dO, causal=True, scale=None, mode=0, stream=None):
+    """Returns (dq, dk, dv), BF16."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream)
+    return dq, dk, dv
+
+
+def tie_stats(q, k, v, o, causal=True, scale=None, mode=0, with_p_one=True, stream=None):
+    """Returns (tie_count, pv_err, p_one or None)."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    tc = torch.empty((B, H, N), device=q.device, dtype=torch.int32)
+    pe = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    po = torch.empty((2, B, H, N), device=q.device, dtype=torch.int32) if with_p_one else None
+    fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, po, stream)
+    return tc, pe, po

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/fa.h declares, and rejects invalid arguments with
+the documented status before touching any device."""
+import ctypes
+import subprocess
+
+import pytest
+
+import __graft_entry__
+
+__graft_entry__.build()
+from precision_flash_attention_attn_gb300 import fa  # noqa: E402
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced: validation fails first
+MISALIGNED = FAKE + 8
+
+
+def test_library_exports_every_declared_symbol():
+    declared = fa.declared_symbols()
+    assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
+                             "fa_profile_start", "fa_profile_stop"}
+    lib = ctypes.CDLL(fa.library_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.library_path()], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(declared) <= exported
+
+
+def test_status_strings():
+    names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_ALLOC", "FA_ERR_CUDA",
+             "FA_ERR_TIMEOUT"]
+    for code, name in enumerate(names):
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def _fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, causal=1, scale=0.125,
+             mode=0, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_fwd(**a)
+
+
+def _bwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=1,
+             N=128, d=64, causal=1, scale=0.125, mode=0, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_bwd(**a)
+
+
+def _stats(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, N=128, d=64, causal=1, scale=0.125, mode=0,
+             tie_count=FAKE, pv_err=FAKE, p_one=None, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_tie_stats(**a)
+
+
+INVALID = [
+    dict(q=0), dict(k=0), dict(v=0), dict(q=MISALIGNED), dict(B=0), dict(H=0), dict(N=0), dict(N=-5),
+    dict(causal=2), dict(causal=-1), dict(mode=3), dict(mode=-1), dict(scale=0.0), dict(scale=-1.0),
+    dict(scale=float("inf")), dict(scale=float("nan")), dict(B=1 << 14, H=1 << 10, N=1024),
+    dict(N=65535 * 128 + 1),
+]
+
+
+@pytest.mark.parametrize("kw", INVALID)
+def test_invalid_arguments_rejected(kw):
+    assert _fwd(**kw) == 1
+    assert _bwd(**kw) == 1
+    assert _stats(**kw) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(o=0), dict(lse=0), dict(o=MISALIGNED)])
+def test_fwd_output_pointers(kw):
+    assert _fwd(**kw) == 1
+
+
+@pytest.mark.parametrize("name", ["dO", "dq", "dk", "dv", "lse", "o"])
+def test_bwd_pointers(name):
+    assert _bwd(**{name: 0}) == 1
+
+
+def test_stats_pointers():
+    assert _stats(tie_count=0) == 1
+    assert _stats(pv_err=0) == 1
+    assert _stats(p_one=MISALIGNED) == 1
+
+
+@pytest.mark.parametrize("d", [32, 96, 256, 100])
+def test_unsupported_head_dim(d):
+    assert _fwd(d=d) == 2
+    assert _bwd(d=d) == 2
+    assert _stats(d=d) == 2
+
+
+def test_binding_raises_on_error():
+    with pytest.raises(fa.FAError) as ei:
+        fa.fa_fwd(0, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 1, 0.125, 0, stream=0)
+    assert ei.value.status == 1

@@ -1,0 +1,109 @@
+"""Forward parity of the CUDA path (C ABI) against the FP64 oracle.
+
+Bounds: max |O_gpu - O_exact| <= 1e-2 (BF16 output) / 2e-3 (FP32 output),
+|LSE_gpu - LSE_exact| <= 1e-4, element by element; causal masking bit-exact."""
+import numpy as np
+import pytest
+
+from conftest import case
+from gpu_helpers import LSE_TOL, dev_bf16, f32, host_f64, o_bound, sample_rows
+from oracle import oracle as orc
+from precision_flash_attention_attn_gb300.inputs import CaseSpec, make_custom
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__
+    __graft_entry__.build()
+    from precision_flash_attention_attn_gb300 import fa as fa_mod
+    return fa_mod
+
+
+def _run(fa, c, mode):
+    q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
+    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
+    assert fa.fa_device_status() == 0
+    return host_f64(o), host_f64(lse)
+
+
+def _check(c, o, lse, mode, rows=None):
+    BH = c.B * c.H
+    qf, kf, vf = (f32(getattr(c, n)).reshape(BH, c.N, c.d) for n in ("q", "k", "v"))
+    ex = orc.fwd(qf, kf, vf, c.causal, c.scale, mode, rows=rows)
+    og = o.reshape(BH * c.N, c.d)
+    lg = lse.reshape(BH * c.N)
+    if rows is not None:
+        og, lg = og[rows], lg[rows]
+    oe = ex["o"].reshape(og.shape)
+    le = ex["lse"].reshape(lg.shape)
+    err = np.abs(og - oe)
+    bound = o_bound(oe, mode)
+    bad = err > bound
+    assert not bad.any(), f"mode {mode}: {bad.sum()} elements over bound, max err {err.max():.3e}"
+    assert np.abs(lg - le).max() <= LSE_TOL, np.abs(lg - le).max()
+    return err.max()
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_tiny_all_rows(fa, mode):
+    c = case("tiny")
+    o, lse = _run(fa, c, mode)
+    _check(c, o, lse, mode)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 200, 384])
+@pytest.mark.parametrize("causal", [True, False])
+def test_shapes_and_tails(fa, d, N, causal):
+    spec = CaseSpec("shape", 2, 2, N, d, causal, 7000 + N + d + int(causal), plant_frac=0.1 if N > 8 else 0.0,
+                    min_plant_row=3)
+    c = make_custom(spec)
+    for mode in (0, 1, 2):
+        o, lse = _run(fa, c, mode)
+        _check(c, o, lse, mode)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_gpt2s_full_size_sampled_rows(fa, mode):
+    c = case("gpt2s")
+    o, lse = _run(fa, c, mode)
+    BH = c.B * c.H
+    planted = np.flatnonzero(c.planted.reshape(-1))
+    rows = sample_rows(BH, c.N, 384, seed=mode, must=planted[::40])
+    _check(c, o, lse, mode, rows=rows)
+
+
+def test_causal_mask_bit_exact(fa):
+    c = case("tiny")
+    q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
+    i = 70
+    rng = np.random.default_rng(11)
+    k2, v2 = c.k.copy(), c.v.copy()
+    noise = rng.integers(0, 1 << 16, size=k2[:, :, i + 1:].shape).astype(np.uint16) & 0x7F7F
+    k2[:, :, i + 1:] ^= noise
+    v2[:, :, i + 1:] ^= noise
+    for mode in (0, 1, 2):
+        o1, l1 = fa.attention_fwd(q, k, v, True, c.scale, mode)
+        o2, l2 = fa.attention_fwd(q, dev_bf16(k2), dev_bf16(v2), True, c.scale, mode)
+        a, b = host_f64(o1), host_f64(o2)
+        assert np.array_equal(a[:, :, : i + 1], b[:, :, : i + 1])
+        assert np.array_equal(host_f64(l1)[:, :, : i + 1], host_f64(l2)[:, :, : i + 1])
+        assert not np.array_equal(a[:, :, i + 1:], b[:, :, i + 1:])
+
+
+def test_identical_keys_give_identical_scores(fa):
+    # Precondition of exact tie counting: copies of one key row at any column
+    # position of a 128-key tile yield bit-identical FP32 scores.
+    rng = np.random.default_rng(12)
+    N, d = 256, 64
+    from precision_flash_attention_attn_gb300.inputs import bf16_bits
+    q = bf16_bits(rng.standard_normal((1, 1, N, d)).astype(np.float32))
+    k = bf16_bits(rng.standard_normal((1, 1, N, d)).astype(np.float32))
+    k[0, 0, :] = k[0, 0, 5]           # every key identical
+    v = bf16_bits(rng.standard_normal((1, 1, N, d)).astype(np.float32))
+    tc, pe, po = fa.tie_stats(dev_bf16(q), dev_bf16(k), dev_bf16(v),
+                              fa.attention_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), False, 0.125, 0)[0],
+                              False, 0.125, 0)
+    assert np.all(tc.cpu().numpy() == N)
