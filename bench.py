@@ -67,6 +67,16 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Maximum of a per-rank float over all ranks (identity without a group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def visible_pairs(B, H, N, causal):
     return B * H * (N * (N + 1) // 2 if causal else N * N)
 
@@ -314,11 +324,7 @@ def run_ours(args):
     for e in ev:
         for i in range(len(MODES)):
             per_mode_ms[i] += e[i].elapsed_time(e[i + 1])
-    total_ms = sum(per_mode_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per_mode_ms), dist, dev)
     ms_step = total_ms / args.steps
     value = world * flop_step * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -348,10 +354,7 @@ def run_ours(args):
         b.synchronize()
         if s >= 2:
             e2e_ms += a.elapsed_time(b)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = world * flop_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
     # ------------------------------------------------------------ roofline --

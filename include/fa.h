@@ -152,6 +152,15 @@ enum {
 int fa_profile_start(void);
 int fa_profile_stop(int n, int64_t* launches, double* total_ms);
 
+/*
+ * Description of the most recent CUDA failure behind an FA_ERR_CUDA (or
+ * FA_ERR_ALLOC) returned on the calling thread: the failing step and the CUDA
+ * error string, e.g. "bwd_main launch: too many resources requested for
+ * launch".  Empty if none.  Thread-local static storage, valid until the next
+ * call on this thread.
+ */
+const char* fa_last_error(void);
+
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(int status);
 

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstdio>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -21,6 +22,8 @@ __device__ int g_fa_status;
 
 constexpr int kMaxDevices = 64;
 
+thread_local char g_last_error[256];
+
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
@@ -31,10 +34,16 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+int cuda_fail(const char* step, cudaError_t e) {
+    fa::set_error(step, e);
+    return FA_ERR_CUDA;
+}
+
 // Current device: sm_103 check and the status word address.
 int device_info(DeviceInfo** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail("cudaGetDevice", ce);
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo& di = g_dev[dev];
@@ -46,7 +55,8 @@ int device_info(DeviceInfo** out) {
         di.supported = (major == 10 && minor == 3);
         if (di.supported) {
             void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+            ce = cudaGetSymbolAddress(&p, g_fa_status);
+            if (ce != cudaSuccess) return cuda_fail("cudaGetSymbolAddress(status word)", ce);
             di.status = static_cast<int*>(p);
         }
         di.probed = true;
@@ -91,14 +101,32 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        char msg[64];
+        snprintf(msg, sizeof msg, "CUresult %d", static_cast<int>(r));
+        fa::set_error_msg("cuTensorMapEncodeTiled", msg);
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
 }
 
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
 }  // namespace
 
+namespace fa {
+
+void set_error_msg(const char* step, const char* msg) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", step, msg);
+}
+
+void set_error(const char* step, cudaError_t e) { set_error_msg(step, cudaGetErrorString(e)); }
+
+}  // namespace fa
+
 extern "C" {
+
+const char* fa_last_error(void) { return g_last_error; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -163,7 +191,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     void* ws = nullptr;
     const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
     if (fail && fail[0] == '1') return FA_ERR_ALLOC;
-    if (cudaMallocAsync(&ws, ws_bytes, st) != cudaSuccess || !ws) {
+    cudaError_t ae = cudaMallocAsync(&ws, ws_bytes, st);
+    if (ae != cudaSuccess || !ws) {
+        fa::set_error("cudaMallocAsync(workspace)", ae);
         cudaGetLastError();
         return FA_ERR_ALLOC;
     }
@@ -206,7 +236,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         a.status = di->status;
         if (fa::launch_bwd(a, st) != cudaSuccess) rc = FA_ERR_CUDA;
     }
-    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == FA_OK) rc = FA_ERR_CUDA;
+    const cudaError_t fe = cudaFreeAsync(ws, st);
+    if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;
 }
 

@@ -463,7 +463,10 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     auto kern = bwd_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+        set_error("bwd_main cudaFuncSetAttribute", e);
+        return e;
+    }
     BwdParams p;
     p.lse2 = a.lse2;
     p.delta = a.delta;
@@ -480,7 +483,9 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     prof_begin(3, stream);
     kern<<<grid, 320, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, p);
     prof_end(3, stream);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) set_error("bwd_main launch", e);
+    return e;
 }
 
 int num_sms() {
@@ -498,7 +503,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
     bwd_pre_kernel<<<sms * 4, 256, 0, stream>>>(a);
     prof_end(2, stream);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+        set_error("bwd_pre launch", e);
+        return e;
+    }
     if (a.d == 64)
         e = a.causal ? launch_main<64, true>(a, stream) : launch_main<64, false>(a, stream);
     else
@@ -508,7 +516,9 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
     prof_begin(4, stream);
     dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8);
     prof_end(4, stream);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) set_error("dq_convert launch", e);
+    return e;
 }
 
 }  // namespace fa

@@ -388,7 +388,10 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using L = FwdLayout<D, MODE>;
     auto kern = fwd_kernel<D, MODE, CAUSAL, STATS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+        set_error("fwd cudaFuncSetAttribute", e);
+        return e;
+    }
     FwdParams p;
     p.o = a.o;
     p.lse = a.lse;
@@ -403,7 +406,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     prof_begin(STATS ? 1 : 0, stream);
     kern<<<grid, 192, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
     prof_end(STATS ? 1 : 0, stream);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) set_error("fwd launch", e);
+    return e;
 }
 
 template <int D, int MODE>

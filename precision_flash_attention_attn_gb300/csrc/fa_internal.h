@@ -58,6 +58,10 @@ struct StatsArgs {
     int* status;
 };
 
+// Record the CUDA error behind a failing step (read back by fa_last_error).
+void set_error(const char* step, cudaError_t e);
+void set_error_msg(const char* step, const char* msg);
+
 // Kernel timing hooks (no-ops unless a profiling session is active).
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);

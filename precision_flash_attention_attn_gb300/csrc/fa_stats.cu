@@ -116,7 +116,9 @@ cudaError_t launch_pv_err(const StatsArgs& a, cudaStream_t stream) {
     else
         pv_err_kernel<128><<<grid, 128, 0, stream>>>(a);
     prof_end(5, stream);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) set_error("pv_err launch", e);
+    return e;
 }
 
 }  // namespace fa

@@ -35,6 +35,8 @@ _lib.fa_tie_stats.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P, _P
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
 _lib.fa_profile_stop.argtypes = [_i, _P, _P]
+_lib.fa_last_error.argtypes = []
+_lib.fa_last_error.restype = ctypes.c_char_p
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
@@ -44,8 +46,13 @@ for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, 
 
 class FAError(RuntimeError):
     def __init__(self, fn, status):
-        super().__init__(f"{fn} returned {status} ({fa_status_string(status)})")
+        detail = fa_last_error() if status in (3, 4) else ""
+        super().__init__(f"{fn} returned {status} ({fa_status_string(status)})" + (f": {detail}" if detail else ""))
         self.status = status
+
+
+def fa_last_error() -> str:
+    return _lib.fa_last_error().decode()
 
 
 def library_path() -> str:

@@ -80,10 +80,11 @@ def test_causal_mask_bit_exact(fa):
     q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
     i = 70
     rng = np.random.default_rng(11)
+    from precision_flash_attention_attn_gb300.inputs import bf16_bits
     k2, v2 = c.k.copy(), c.v.copy()
-    noise = rng.integers(0, 1 << 16, size=k2[:, :, i + 1:].shape).astype(np.uint16) & 0x7F7F
-    k2[:, :, i + 1:] ^= noise
-    v2[:, :, i + 1:] ^= noise
+    shape = k2[:, :, i + 1:].shape
+    k2[:, :, i + 1:] = bf16_bits(rng.standard_normal(shape).astype(np.float32) * 4)
+    v2[:, :, i + 1:] = bf16_bits(rng.standard_normal(shape).astype(np.float32) * 4)
     for mode in (0, 1, 2):
         o1, l1 = fa.attention_fwd(q, k, v, True, c.scale, mode)
         o2, l2 = fa.attention_fwd(q, dev_bf16(k2), dev_bf16(v2), True, c.scale, mode)
