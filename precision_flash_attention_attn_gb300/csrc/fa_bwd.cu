@@ -29,6 +29,8 @@
 //   dq_convert_kernel  dQ workspace (FP32) -> BF16.
 #include <cuda_bf16.h>
 
+#include <cstdio>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -142,7 +144,7 @@ struct BwdParams {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dqacc, const BwdParams p) {
@@ -484,7 +486,17 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     kern<<<grid, 320, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, p);
     prof_end(3, stream);
     e = cudaGetLastError();
-    if (e != cudaSuccess) set_error("bwd_main launch", e);
+    if (e != cudaSuccess) {
+        cudaFuncAttributes fa_attr{};
+        char msg[200];
+        if (cudaFuncGetAttributes(&fa_attr, kern) == cudaSuccess)
+            snprintf(msg, sizeof msg, "%s (regs %d, max threads %d, local %zu B, dyn smem %d B)",
+                     cudaGetErrorString(e), fa_attr.numRegs, fa_attr.maxThreadsPerBlock,
+                     fa_attr.localSizeBytes, L::kAlloc);
+        else
+            snprintf(msg, sizeof msg, "%s", cudaGetErrorString(e));
+        set_error_msg("bwd_main launch", msg);
+    }
     return e;
 }
 
