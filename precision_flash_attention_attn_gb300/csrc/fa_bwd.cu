@@ -39,39 +39,59 @@ namespace {
 
 // ------------------------------------------------------------- preprocess --
 
+// D/8 threads per row, 8 elements (16 bytes of dO) each; rows padded to Npad.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
-    const int warps_total = gridDim.x * (blockDim.x >> 5);
-    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    constexpr int TPR = D / 8;       // threads per row
+    constexpr int RPW = 32 / TPR;    // rows per warp and pass
     const int lane = threadIdx.x & 31;
+    const int sub = lane % TPR;
     const long long rows = static_cast<long long>(a.BH) * a.Npad;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
-    for (long long r = gw; r < rows; r += warps_total) {
+    for (long long r0 = gw * RPW; r0 < rows; r0 += nwarps * RPW) {
+        const long long r = r0 + lane / TPR;
         const int bh = static_cast<int>(r / a.Npad);
         const int i = static_cast<int>(r % a.Npad);
+        const bool valid = r < rows && i < a.N;
         float acc = 0.f;
-        float l2 = INFINITY;  // padded rows: P = exp2(s - inf) = 0
-        if (i < a.N) {
-            const size_t base = (static_cast<size_t>(bh) * a.N + i) * a.d;
-            for (int c = lane; c < a.d; c += 32) {
-                const float g = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dout)[base + c]);
-                const float o = (a.mode == 2) ? static_cast<const float*>(a.o)[base + c]
-                                              : __bfloat162float(static_cast<const __nv_bfloat16*>(a.o)[base + c]);
-                acc = fmaf(g, o, acc);
-            }
+        if (valid) {
+            const size_t base = (static_cast<size_t>(bh) * a.N + i) * D + sub * 8;
+            const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + base);
+            const uint32_t gw4[4] = {g.x, g.y, g.z, g.w};
+            if (a.mode == 2) {
+                const float4 o0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + base);
+                const float4 o1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + base + 4);
+                const float of[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            l2 = a.lse[static_cast<size_t>(bh) * a.N + i] * log2e;
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(__uint_as_float(gw4[e] << 16), of[2 * e], acc);
+                    acc = fmaf(__uint_as_float(gw4[e] & 0xFFFF0000u), of[2 * e + 1], acc);
+                }
+            } else {
+                const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + base);
+                const uint32_t ow4[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc = fmaf(__uint_as_float(gw4[e] << 16), __uint_as_float(ow4[e] << 16), acc);
+                    acc = fmaf(__uint_as_float(gw4[e] & 0xFFFF0000u), __uint_as_float(ow4[e] & 0xFFFF0000u), acc);
+                }
+            }
         }
-        if (lane == 0) {
-            a.delta[r] = (i < a.N) ? acc : 0.f;
-            a.lse2[r] = l2;
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (sub == 0 && r < rows) {
+            a.delta[r] = valid ? acc : 0.f;
+            // padded rows: P = exp2(s - inf) = 0
+            a.lse2[r] = valid ? a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : INFINITY;
         }
     }
     // zero the dQ accumulator
-    const size_t n4 = static_cast<size_t>(a.BH) * a.N * a.d / 4;
+    const size_t n4 = static_cast<size_t>(a.BH) * a.N * D / 4;
     float4* acc4 = reinterpret_cast<float4*>(a.dq_acc);
-    for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
-         e += static_cast<size_t>(gridDim.x) * blockDim.x)
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += stride)
         acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -512,7 +532,10 @@ int num_sms() {
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
     const int sms = num_sms();
     prof_begin(2, stream);
-    bwd_pre_kernel<<<sms * 4, 256, 0, stream>>>(a);
+    if (a.d == 64)
+        bwd_pre_kernel<64><<<sms * 4, 256, 0, stream>>>(a);
+    else
+        bwd_pre_kernel<128><<<sms * 4, 256, 0, stream>>>(a);
     prof_end(2, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

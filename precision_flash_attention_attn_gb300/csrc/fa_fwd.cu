@@ -11,18 +11,21 @@
 // to M, m = beta*M if M > 0 and C > 1, 0 if M < 0 and C > 1, else M (ties are
 // exact equality of FP32 raw scores, eps = 0).
 //
-// One CTA owns a 128-row query tile of one (batch, head) and streams 128-key
-// K/V tiles.  Warp roles:
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t).  Reads S from
-//              TMEM, masks, reduces row max and tie count, updates the shift,
-//              exponentiates (ex2), writes BF16 Pbar to swizzled shared
-//              memory, rescales the O accumulator in TMEM when the shift
-//              changes, and finally normalises and stores O and the LSE.
-//   warp 4     TMA producer: Q once, then K and V tiles through a ring.
-//   warp 5     MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers, then
-//              O += Pbar_j V_j into the TMEM O accumulator (tcgen05.mma,
-//              kind::f16, A and B from shared memory).
-// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256,256+d) O.
+// One CTA owns NQ (1 or 2) consecutive 128-row query tiles of one (batch,
+// head) and streams 128-key K/V tiles shared by them.  Warp roles:
+//   warps 4t..4t+3  softmax of query tile t: thread r owns row r (TMEM lane
+//              r).  Reads S from TMEM (and frees it at once), masks, reduces
+//              the row max and tie count, updates the shift, waits for the
+//              previous Pbar V product, rescales the O accumulator in TMEM
+//              when the shift changed, exponentiates (ex2) while writing BF16
+//              Pbar to swizzled shared memory, and finally normalises and
+//              stores O and the LSE.
+//   warp 4*NQ  TMA producer: the Q tiles once, then K and V tiles in a ring.
+//   warp 4*NQ+1  MMA issuer: S_t = Q_t K_j^T into tile t's TMEM S buffer,
+//              then O_t += Pbar_t V_j (tcgen05.mma kind::f16, A and B from
+//              shared memory).  With two query tiles the two softmax
+//              warpgroups overlap each other's MMAs and share every K/V tile.
+// TMEM columns: S_t at 128*t, O_t at 128*NQ + d*t.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -31,34 +34,38 @@
 namespace fa {
 namespace {
 
-template <int D, int MODE>
+template <int D, int MODE, int NQ>
 struct FwdLayout {
     static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows x D BF16
-    static constexpr int kStages = (D == 64) ? 3 : 2;
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kP = kV + kStages * kTileBytes;
+    static constexpr int kStages = (D == 64) ? ((NQ == 2 && MODE == 2) ? 2 : 3) : 2;
     static constexpr int kPBytes = kBlockM * kBlockN * 2;
+    static constexpr int kQ = 0;                                  // [NQ]
+    static constexpr int kK = kQ + NQ * kTileBytes;               // [kStages]
+    static constexpr int kV = kK + kStages * kTileBytes;          // [kStages]
+    static constexpr int kP = kV + kStages * kTileBytes;          // [NQ]
     // FP32-output mode feeds Pbar to the tensor core as hi + lo BF16 parts
-    static constexpr int kPLo = kP + kPBytes;
-    static constexpr int kBar = kPLo + (MODE == 2 ? kPBytes : 0);
+    static constexpr int kPLo = kP + NQ * kPBytes;                // [NQ], mode 2
+    static constexpr int kBar = kPLo + (MODE == 2 ? NQ * kPBytes : 0);
     // barriers
     static constexpr int kQFull = 0;
     static constexpr int kKFull = 1;
     static constexpr int kVFull = kKFull + kStages;
     static constexpr int kKVEmpty = kVFull + kStages;
-    static constexpr int kSFull = kKVEmpty + kStages;  // 2
-    static constexpr int kSEmpty = kSFull + 2;         // 2
-    static constexpr int kPFull = kSEmpty + 2;
-    static constexpr int kODone = kPFull + 1;
-    static constexpr int kDrain = kODone + 1;
+    static constexpr int kSFull = kKVEmpty + kStages;  // [NQ]
+    static constexpr int kSEmpty = kSFull + NQ;        // [NQ]
+    static constexpr int kPFull = kSEmpty + NQ;        // [NQ]
+    static constexpr int kODone = kPFull + NQ;         // [NQ]
+    static constexpr int kDrain = kODone + NQ;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kOCol = 256;
+    static constexpr uint32_t kTmemUsed = NQ * (128 + D);
+    static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static constexpr uint32_t kSCol = 0;
+    static constexpr uint32_t kOCol = 128 * NQ;
+    static constexpr int kThreads = 128 * NQ + 64;
+    static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
@@ -71,12 +78,14 @@ struct FwdParams {
     int* status;
 };
 
-template <int D, int MODE, bool CAUSAL, bool STATS>
-__global__ void __launch_bounds__(192, 1)
+template <int D, int MODE, bool CAUSAL, bool STATS, int NQ>
+__global__ void __launch_bounds__(128 * NQ + 64, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using L = FwdLayout<D, MODE>;
+    using L = FwdLayout<D, MODE, NQ>;
     constexpr int S = L::kStages;
+    constexpr int kProducerWarp = 4 * NQ;
+    constexpr int kMmaWarp = 4 * NQ + 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -86,10 +95,20 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
-    const int qt = gridDim.y - 1 - blockIdx.y;  // longest causal tiles first
-    const int q0 = qt * kBlockM;
+    const int cq = gridDim.y - 1 - blockIdx.y;  // longest causal tiles first
     const int n_ktiles_all = (p.N + kBlockN - 1) / kBlockN;
-    const int n_kt = CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all;
+    // per query tile: first row and number of key tiles it visits (0: past N)
+    int q0s[NQ], nkts[NQ];
+    int n_kt = 0, n_active = 0;
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+        const int qt = cq * NQ + t;
+        q0s[t] = qt * kBlockM;
+        const bool active = q0s[t] < p.N;
+        nkts[t] = !active ? 0 : (CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all);
+        n_kt = nkts[t] > n_kt ? nkts[t] : n_kt;
+        n_active += active ? 1 : 0;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kQFull), 1);
@@ -98,16 +117,16 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(L::kVFull + s), 1);
             mbar_init(bar(L::kKVEmpty + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(L::kSFull + b), 1);
-            mbar_init(bar(L::kSEmpty + b), 128);
+        for (int t = 0; t < NQ; ++t) {
+            mbar_init(bar(L::kSFull + t), 1);
+            mbar_init(bar(L::kSEmpty + t), 128);
+            mbar_init(bar(L::kPFull + t), 128);
+            mbar_init(bar(L::kODone + t), 1);
         }
-        mbar_init(bar(L::kPFull), 128);
-        mbar_init(bar(L::kODone), 1);
         mbar_init(bar(L::kDrain), 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
         tmem_relinquish();
     }
@@ -116,15 +135,19 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(L::kQFull), L::kTileBytes);
-            for (int b = 0; b < D / 64; ++b)
-                tma_load_3d(sb + L::kQ + b * 16384, &tm_q, bar(L::kQFull), b * 64, q0, bh);
+            mbar_arrive_expect_tx(bar(L::kQFull), L::kTileBytes * n_active);
+            for (int t = 0; t < NQ; ++t) {
+                if (nkts[t] == 0) continue;
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(sb + L::kQ + t * L::kTileBytes + b * 16384, &tm_q, bar(L::kQFull), b * 64, q0s[t],
+                                bh);
+            }
             int issued = 0;
             for (int j = 0; j < n_kt; ++j) {
                 const int s = j % S;
@@ -149,65 +172,82 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_wait(bar(L::kVFull + j % S), u & 1u, p.status);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
             constexpr uint32_t kIdPV = idesc_bf16(kBlockM, D, false, true);
             bool ok = mbar_wait(bar(L::kQFull), 0, p.status);
-            auto issue_pv = [&](int t) {
-                const int s = t % S;
-                const uint32_t u = static_cast<uint32_t>(t / S);
+            auto issue_pv = [&](int jj) {
+                const int s = jj % S;
+                const uint32_t u = static_cast<uint32_t>(jj / S);
                 ok = ok && mbar_wait(bar(L::kVFull + s), u & 1u, p.status);
-                ok = ok && mbar_wait(bar(L::kPFull), static_cast<uint32_t>(t) & 1u, p.status);
-                if (!ok) return;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(sb + L::kP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                    mma_bf16_ss(tmem + L::kOCol, a, b, kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (MODE == 2) {
+                for (int t = 0; t < NQ; ++t) {
+                    if (jj >= nkts[t]) continue;
+                    ok = ok && mbar_wait(bar(L::kPFull + t), static_cast<uint32_t>(jj) & 1u, p.status);
+                    if (!ok) return;
+                    tc_fence_after();
+                    const uint32_t o_t = tmem + L::kOCol + t * D;
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t a = sdesc_sw128(sb + L::kPLo + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t a =
+                            sdesc_sw128(sb + L::kP + t * L::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                         const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                        mma_bf16_ss(tmem + L::kOCol, a, b, kIdPV, 1u);
+                        mma_bf16_ss(o_t, a, b, kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
+                    if (MODE == 2) {
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                            const uint64_t a = sdesc_sw128(
+                                sb + L::kPLo + t * L::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
+                            mma_bf16_ss(o_t, a, b, kIdPV, 1u);
+                        }
+                    }
+                    mma_commit(bar(L::kODone + t));
                 }
-                mma_commit(bar(L::kODone));
-                mma_commit(bar(L::kKVEmpty + s));
+                if (ok) mma_commit(bar(L::kKVEmpty + s));
             };
             for (int j = 0; j < n_kt && ok; ++j) {
                 const int s = j % S;
                 const uint32_t u = static_cast<uint32_t>(j / S);
-                const int buf = j & 1;
                 ok = mbar_wait(bar(L::kKFull + s), u & 1u, p.status);
-                if (ok && j >= 2)
-                    ok = mbar_wait(bar(L::kSEmpty + buf), static_cast<uint32_t>((j >> 1) - 1) & 1u, p.status);
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(sb + L::kQ + koff, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sb + L::kK + s * L::kTileBytes + koff, 16, 1024);
-                    mma_bf16_ss(tmem + buf * 128, a, b, kIdS, kk > 0 ? 1u : 0u);
+                for (int t = 0; t < NQ; ++t) {
+                    if (!ok || j >= nkts[t]) continue;
+                    if (j >= 1)
+                        ok = mbar_wait(bar(L::kSEmpty + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint64_t a = sdesc_sw128(sb + L::kQ + t * L::kTileBytes + koff, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sb + L::kK + s * L::kTileBytes + koff, 16, 1024);
+                        mma_bf16_ss(tmem + L::kSCol + t * 128, a, b, kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(L::kSFull + t));
                 }
-                mma_commit(bar(L::kSFull + buf));
-                if (j >= 1) issue_pv(j - 1);
+                if (ok && j >= 1) issue_pv(j - 1);
             }
-            if (ok) issue_pv(n_kt - 1);
+            if (ok && n_kt > 0) issue_pv(n_kt - 1);
             // Drain: every MMA issued above has completed before TMEM is freed.
             mma_commit(bar(L::kDrain));
             mbar_wait(bar(L::kDrain), 0, p.status);
         }
     } else {
         // ---------------------------------------------------------- softmax
-        const int row = threadIdx.x;  // 0..127 == TMEM lane
+        const int t = warp >> 2;               // query tile of this warpgroup
+        const int row = threadIdx.x & 127;     // == TMEM lane
+        const int q0 = q0s[t];
+        const int nkt = nkts[t];
         const int qrow = q0 + row;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_off + L::kSCol + t * 128;
+        const uint32_t o_tm = tmem + lane_off + L::kOCol + t * D;
+        const uint32_t p_sm = sb + L::kP + t * L::kPBytes;
+        const uint32_t plo_sm = sb + L::kPLo + t * L::kPBytes;
         const float sl2 = p.scale_log2;
         float M = -INFINITY;  // running max of raw scores
         int C = 0;            // running count of keys equal to M
@@ -216,22 +256,23 @@ __global__ void __launch_bounds__(192, 1)
         float l = 0.f;
         int ones0 = 0, ones1 = 0;
         bool ok = true;
-        for (int j = 0; j < n_kt; ++j) {
-            const int buf = j & 1;
-            ok = mbar_wait(bar(L::kSFull + buf), static_cast<uint32_t>(j >> 1) & 1u, p.status);
+        for (int j = 0; j < nkt; ++j) {
+            ok = mbar_wait(bar(L::kSFull + t), static_cast<uint32_t>(j) & 1u, p.status);
             if (!ok) break;
             tc_fence_after();
             float s[kBlockN];
+            {
+                uint32_t r[kBlockN / 32][32];
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + buf * 128 + c * 32, r);
-                tmem_wait_ld();
+                for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(s_tm + c * 32, r[c]);
+                tmem_wait_ld();  // one wait for all four loads
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+                for (int c = 0; c < kBlockN / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
             }
             tc_fence_before();
-            mbar_arrive(bar(L::kSEmpty + buf));
+            mbar_arrive(bar(L::kSEmpty + t));  // S is in registers: the next S may land
 
             const int k0 = j * kBlockN;
             const bool need_mask = CAUSAL ? (k0 + kBlockN > q0) : (k0 + kBlockN > p.N);
@@ -265,73 +306,64 @@ __global__ void __launch_bounds__(192, 1)
             const float mc_new = m_new * sl2;
             const bool changed = (m_new != m);
             const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
-            float lsum = 0.f;
-            uint32_t pk[kBlockN / 2];
-            uint32_t pl[kBlockN / 2];  // unused (and eliminated) unless MODE == 2
-#pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -mc_new));
-                const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -mc_new));
-                lsum += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-                if (MODE == 2) {
-                    // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
-                    const float h0 = __uint_as_float(pk[c] << 16);
-                    const float h1 = __uint_as_float(pk[c] & 0xFFFF0000u);
-                    pl[c] = pack_bf16x2(p0 - h0, p1 - h1);
-                }
-            }
-            l = l * rsc + lsum;
             m = m_new;
             mc = mc_new;
-            if (STATS) {
-                int cnt = 0;
+            // Pbar_j may overwrite the shared P buffer and O may be rescaled
+            // only after O += Pbar_{j-1} V_{j-1} has completed.
+            if (j >= 1) {
+                ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
+                if (!ok) break;
+            }
+            float lsum = 0.f;
+            int cnt = 0;
 #pragma unroll
-                for (int c = 0; c < kBlockN / 2; ++c)
-                    cnt += ((pk[c] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[c] >> 16) == 0x3F80u ? 1 : 0);
+            for (int ch = 0; ch < kBlockN / 8; ++ch) {
+                uint32_t w[4], wl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[ch * 8 + 2 * e], sl2, -mc_new));
+                    const float p1 = ex2_approx(fmaf(s[ch * 8 + 2 * e + 1], sl2, -mc_new));
+                    lsum += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
+                    if (MODE == 2) {
+                        // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
+                        const float h0 = __uint_as_float(w[e] << 16);
+                        const float h1 = __uint_as_float(w[e] & 0xFFFF0000u);
+                        wl[e] = pack_bf16x2(p0 - h0, p1 - h1);
+                    }
+                    if (STATS)
+                        cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
+                }
+                const uint32_t off = (ch >> 3) * 16384 + sw128_off(row, ch & 7);
+                st_shared_v4(p_sm + off, w[0], w[1], w[2], w[3]);
+                if (MODE == 2) st_shared_v4(plo_sm + off, wl[0], wl[1], wl[2], wl[3]);
+            }
+            l = l * rsc + lsum;
+            if (STATS) {
                 if (changed) ones1 = 0;
                 ones0 += cnt;
                 ones1 += cnt;
             }
-            // Pbar_j may overwrite the shared P buffer and O may be rescaled
-            // only after O += Pbar_{j-1} V_{j-1} has completed.
-            if (j >= 1) {
-                ok = mbar_wait(bar(L::kODone), static_cast<uint32_t>(j - 1) & 1u, p.status);
-                if (!ok) break;
-            }
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch)
-                st_shared_v4(sb + L::kP + (ch >> 3) * 16384 + sw128_off(row, ch & 7), pk[4 * ch],
-                             pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            if (MODE == 2) {
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch)
-                    st_shared_v4(sb + L::kPLo + (ch >> 3) * 16384 + sw128_off(row, ch & 7),
-                                 pl[4 * ch],
-                                 pl[4 * ch + 1],
-                                 pl[4 * ch + 2],
-                                 pl[4 * ch + 3]);
-            }
+            // rescale O after the scores are consumed (keeps register use low)
             if (j >= 1 && __any_sync(0xffffffffu, changed)) {
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
-                    const uint32_t ta = tmem + lane_off + L::kOCol + c * 32;
-                    tmem_ld32(ta, r);
+                    tmem_ld32(o_tm + c * 32, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
-                    tmem_st32(ta, r);
+                    tmem_st32(o_tm + c * 32, r);
                 }
                 tmem_wait_st();
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(L::kPFull));
+            mbar_arrive(bar(L::kPFull + t));
         }
-        if (ok) ok = mbar_wait(bar(L::kODone), static_cast<uint32_t>(n_kt - 1) & 1u, p.status);
-        const bool store = ok && qrow < p.N;
+        if (ok && nkt > 0) ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(nkt - 1) & 1u, p.status);
+        const bool store = ok && nkt > 0 && qrow < p.N;
         const size_t rowid = static_cast<size_t>(bh) * p.N + qrow;
         if (STATS) {
             if (store) {
@@ -341,14 +373,14 @@ __global__ void __launch_bounds__(192, 1)
                     p.p_one[static_cast<size_t>(p.BH) * p.N + rowid] = ones1;
                 }
             }
-        } else if (__all_sync(0xffffffffu, ok)) {
+        } else if (nkt > 0 && __all_sync(0xffffffffu, ok)) {
             // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
             tc_fence_after();
             const float inv_l = 1.f / l;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kOCol + c * 32, r);
+                tmem_ld32(o_tm + c * 32, r);
                 tmem_wait_ld();
                 if (!store) continue;
                 if (MODE == 2) {
@@ -377,16 +409,21 @@ __global__ void __launch_bounds__(192, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
+// Two query tiles per CTA where shared memory allows it (d = 64).
+template <int D>
+constexpr int kQTilesPerCta = (D == 64) ? 2 : 1;
+
 template <int D, int MODE, bool CAUSAL, bool STATS>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
-    using L = FwdLayout<D, MODE>;
-    auto kern = fwd_kernel<D, MODE, CAUSAL, STATS>;
+    constexpr int NQ = kQTilesPerCta<D>;
+    using L = FwdLayout<D, MODE, NQ>;
+    auto kern = fwd_kernel<D, MODE, CAUSAL, STATS, NQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) {
         set_error("fwd cudaFuncSetAttribute", e);
@@ -402,9 +439,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
-    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_qt));
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>((n_qt + NQ - 1) / NQ));
     prof_begin(STATS ? 1 : 0, stream);
-    kern<<<grid, 192, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
     prof_end(STATS ? 1 : 0, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) set_error("fwd launch", e);
