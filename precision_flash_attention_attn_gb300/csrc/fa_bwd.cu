@@ -10,8 +10,8 @@
 //   dQ    = dS K,   dK = dS^T Q,   dV = P^T dO   (dK, dV: textbook gradients)
 //
 // Kernels, in stream order:
-//   bwd_pre_kernel   delta and LSE*log2(e) per row into padded workspaces,
-//                    zero the FP32 dQ accumulator.
+//   bwd_pre_kernel   -LSE*log2(e) and -alpha*delta per row into padded
+//                    workspaces, zero the FP32 dQ accumulator.
 //   bwd_kernel       one CTA per (batch*head, 128-key tile); K and V stay in
 //                    shared memory while the CTA walks the 128-query tiles
 //                    (causal: only tiles at or below the diagonal).  Per query
@@ -22,10 +22,14 @@
 //                      dK  += dS^T Q     (TMEM accumulator)
 //                      dQ_t = dS K       (TMEM), added to the FP32 workspace
 //                                        with TMA reduce-add
-//                    Warp roles: warps 0-3 recompute P^T and dS^T (thread t
-//                    owns key row t) and finally store dK, dV; warps 4-7 drain
-//                    dQ tiles from TMEM into the reduce-add; warp 8 issues TMA
-//                    loads; warp 9 issues the MMAs.
+//                    Warp roles: two math warpgroups (warps 0-3: query
+//                    columns 0-63 of the tile, warps 4-7: columns 64-127;
+//                    thread t of a warpgroup owns key row t) recompute P^T and
+//                    dS^T, drain each dQ tile from TMEM into the reduce-add
+//                    (one 32-row box per warp), and finally store dK and dV;
+//                    warp 8 issues TMA loads; warp 9 issues the MMAs.  The
+//                    next tile's S^T and dP^T are issued ahead of the current
+//                    tile's dK/dQ products.
 //   dq_convert_kernel  dQ workspace (FP32) -> BF16.
 #include <cuda_bf16.h>
 
@@ -82,9 +86,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (sub == 0 && r < rows) {
-            a.delta[r] = valid ? acc : 0.f;
+            // stored pre-negated / pre-scaled for the main kernel's FMAs:
+            //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
+            //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
+            a.delta[r] = valid ? -a.scale * acc : 0.f;
             // padded rows: P = exp2(s - inf) = 0
-            a.lse2[r] = valid ? a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : INFINITY;
+            a.lse2[r] = valid ? -a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : -INFINITY;
         }
     }
     // zero the dQ accumulator
@@ -122,9 +129,9 @@ struct BwdLayout {
     static constexpr int kDO = kQ + kQStages * kTile;           // [kQStages]
     static constexpr int kPt = kDO + kQStages * kTile;          // 128 keys x 128 queries BF16
     static constexpr int kDSt = kPt + kBlockM * kBlockN * 2;
-    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2; // 4 warps x 2 x (32 x 32 FP32), swizzled
-    static constexpr int kLse = kStage + 4 * 2 * 4096;          // [kQStages][128] FP32
-    static constexpr int kDelta = kLse + kQStages * 512;        // [kQStages][128] FP32
+    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2; // 8 warps x (32 x 32 FP32), swizzled
+    static constexpr int kLse = kStage + 8 * 4096;              // [kQStages][128] FP32 (-LSE*log2e)
+    static constexpr int kDelta = kLse + kQStages * 512;        // [kQStages][128] FP32 (-alpha*delta)
     static constexpr int kBar = kDelta + kQStages * 512;
     // barriers
     static constexpr int kKVFull = 0;
@@ -144,6 +151,7 @@ struct BwdLayout {
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 232448, "shared memory budget");
     // TMEM columns
     static constexpr uint32_t kColS = 0;
     static constexpr uint32_t kColDP = 128;
@@ -151,6 +159,7 @@ struct BwdLayout {
     static constexpr uint32_t kColDK = 256 + D;
     static constexpr bool kDQAliasS = (D != 64);  // no room for a separate dQ tile at d = 128
     static constexpr uint32_t kColDQ = kDQAliasS ? kColS : 256 + 2 * D;
+    static constexpr uint32_t kMathThreads = 256;  // two warpgroups
 };
 
 struct BwdParams {
@@ -192,14 +201,14 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(bar(L::kQEmpty + s), 1);
         }
         mbar_init(bar(L::kSFull), 1);
-        mbar_init(bar(L::kSEmpty), 128);
+        mbar_init(bar(L::kSEmpty), L::kMathThreads);
         mbar_init(bar(L::kDPFull), 1);
-        mbar_init(bar(L::kDPEmpty), 128);
-        mbar_init(bar(L::kPFull), 128);
-        mbar_init(bar(L::kDSFull), 128);
+        mbar_init(bar(L::kDPEmpty), L::kMathThreads);
+        mbar_init(bar(L::kPFull), L::kMathThreads);
+        mbar_init(bar(L::kDSFull), L::kMathThreads);
         mbar_init(bar(L::kPDSFree), 1);
         mbar_init(bar(L::kDQFull), 1);
-        mbar_init(bar(L::kDQEmpty), 128);
+        mbar_init(bar(L::kDQEmpty), L::kMathThreads);
         mbar_init(bar(L::kDKVDone), 1);
         fence_mbar_init();
     }
@@ -251,19 +260,16 @@ __global__ void __launch_bounds__(320, 1)
             constexpr uint32_t kIdAcc = idesc_bf16(kBlockM, D, false, true);         // dV, dK
             constexpr uint32_t kIdDQ = idesc_bf16(kBlockM, D, true, true);           // dQ
             bool ok = mbar_wait(bar(L::kKVFull), 0, p.status);
-            for (int it = 0; it < n_iter && ok; ++it) {
+            // S^T(it) = K Q^T
+            auto issue_s = [&](int it) {
                 const int s = it % QS;
-                const uint32_t u = static_cast<uint32_t>(it / QS);
-                const uint32_t prev = static_cast<uint32_t>(it - 1) & 1u;
-                const uint32_t cur = static_cast<uint32_t>(it) & 1u;
-                ok = mbar_wait(bar(L::kQFull + s), u & 1u, p.status);
-                if (ok && it >= 1) ok = mbar_wait(bar(L::kSEmpty), prev, p.status);
-                if (ok && it >= 1 && L::kDQAliasS) ok = mbar_wait(bar(L::kDQEmpty), prev, p.status);
-                if (!ok) break;
+                ok = ok && mbar_wait(bar(L::kQFull + s), static_cast<uint32_t>(it / QS) & 1u, p.status);
+                if (ok && it >= 1) ok = mbar_wait(bar(L::kSEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+                if (ok && it >= 1 && L::kDQAliasS)
+                    ok = mbar_wait(bar(L::kDQEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+                if (!ok) return;
                 tc_fence_after();
                 const uint32_t sQ = sb + L::kQ + s * L::kTile;
-                const uint32_t sDO = sb + L::kDO + s * L::kTile;
-                // S^T = K Q^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -271,10 +277,14 @@ __global__ void __launch_bounds__(320, 1)
                                 kIdSS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(L::kSFull));
-                // dP^T = V dO^T
-                if (it >= 1) ok = mbar_wait(bar(L::kDPEmpty), prev, p.status);
-                if (!ok) break;
+            };
+            // dP^T(it) = V dO^T   (Q/dO stage it is already known to be loaded)
+            auto issue_dp = [&](int it) {
+                const int s = it % QS;
+                if (ok && it >= 1) ok = mbar_wait(bar(L::kDPEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+                if (!ok) return;
                 tc_fence_after();
+                const uint32_t sDO = sb + L::kDO + s * L::kTile;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -282,6 +292,20 @@ __global__ void __launch_bounds__(320, 1)
                                 kIdSS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(L::kDPFull));
+            };
+            // Software pipeline: the next tile's S^T (and dP^T) are issued
+            // ahead of this tile's dK/dQ products, so the P^T/dS^T warps find
+            // their next scores ready.  With dQ aliasing S^T (d = 128) the next
+            // S^T must instead wait for this tile's dQ to be drained.
+            if (n_iter > 0) {
+                issue_s(0);
+                issue_dp(0);
+            }
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int s = it % QS;
+                const uint32_t cur = static_cast<uint32_t>(it) & 1u;
+                const uint32_t sQ = sb + L::kQ + s * L::kTile;
+                const uint32_t sDO = sb + L::kDO + s * L::kTile;
                 // dV += P^T dO
                 ok = mbar_wait(bar(L::kPFull), cur, p.status);
                 if (!ok) break;
@@ -292,6 +316,8 @@ __global__ void __launch_bounds__(320, 1)
                     const uint64_t b = sdesc_sw128(sDO + kk * 2048, 16384, 1024);
                     mma_bf16_ss(tmem + L::kColDV, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
                 }
+                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(it + 1);
+                if (!ok) break;
                 // dK += dS^T Q
                 ok = mbar_wait(bar(L::kDSFull), cur, p.status);
                 if (!ok) break;
@@ -303,7 +329,7 @@ __global__ void __launch_bounds__(320, 1)
                     mma_bf16_ss(tmem + L::kColDK, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 // dQ_t = dS K  (A = dS^T buffer read M-major, B = K read N-major)
-                if (!L::kDQAliasS && it >= 1) ok = mbar_wait(bar(L::kDQEmpty), prev, p.status);
+                if (!L::kDQAliasS && it >= 1) ok = mbar_wait(bar(L::kDQEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -315,89 +341,167 @@ __global__ void __launch_bounds__(320, 1)
                 mma_commit(bar(L::kDQFull));
                 mma_commit(bar(L::kQEmpty + s));
                 mma_commit(bar(L::kPDSFree));
+                if (it + 1 < n_iter) {
+                    if (L::kDQAliasS) issue_s(it + 1);
+                    issue_dp(it + 1);
+                }
             }
             mma_commit(bar(L::kDKVDone));
             mbar_wait(bar(L::kDKVDone), 0, p.status);
         }
-    } else if (warp < 4) {
-        // -------------------------------------------- P^T and dS^T (key rows)
-        const int kr = threadIdx.x;  // key row within the tile == TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const float sl2 = p.scale_log2;
+    } else {
+        // ------------------------- math warpgroups: P^T, dS^T, dQ drain, dK/dV
+        const int wg = warp >> 2;             // 0: query columns 0-63, 1: 64-127
+        const int wq = warp & 3;              // TMEM lane quarter
+        const int kr = threadIdx.x & 127;     // key row within the tile == TMEM lane
+        const int c0 = wg * 64;               // first query column of this warpgroup
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t alx2 = f2_pack(p.scale, p.scale);
+        const uint32_t stage = sb + L::kStage + (warp & 7) * 4096;
         bool ok = true;
+
+        // Drain dQ of query tile `jt`: this warp's 32 query rows, this
+        // warpgroup's half of the d columns, as 32 x 32 FP32 boxes added into
+        // the workspace with TMA reduce-add.
+        auto drain_dq = [&](int jt) -> bool {
+            bool good = mbar_wait(bar(L::kDQFull), static_cast<uint32_t>(jt) & 1u, p.status);
+            if (!__all_sync(0xffffffffu, good)) return false;
+            tc_fence_after();
+            const int q0 = (qt_begin + jt) * kBlockM;
+#pragma unroll
+            for (int cb = 0; cb < D / 64; ++cb) {
+                const int col = wg * (D / 2) + cb * 32;
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + L::kColDQ + col, r);
+                tmem_wait_ld();
+                if (cb == D / 64 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kDQEmpty));
+                }
+                if (lane == 0) bulk_wait_read0();  // this warp's previous reduce has read its box
+                __syncwarp();
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(stage + sw128_off(lane, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2], r[4 * ch + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_3d(&tm_dqacc, stage, col, q0 + wq * 32, bh);
+                    bulk_commit();
+                }
+            }
+            return true;
+        };
+
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % QS;
             const uint32_t u = static_cast<uint32_t>(it / QS);
             const uint32_t cur = static_cast<uint32_t>(it) & 1u;
             const int qt = qt_begin + it;
-            ok = mbar_wait(bar(L::kSFull), cur, p.status) && mbar_wait(bar(L::kQFull + s), u & 1u, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            const float* lse2 = reinterpret_cast<const float*>(smem + L::kLse + s * 512);
-            const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * 512);
-            float pr[kBlockM];
-#pragma unroll
-            for (int c = 0; c < kBlockM / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kColS + c * 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) pr[c * 32 + e] = __uint_as_float(r[e]);
+            if (L::kDQAliasS && it >= 1) {
+                // dQ shares the S^T columns: drain it before the next S^T lands
+                ok = drain_dq(it - 1);
+                if (!ok) break;
             }
-            tc_fence_before();
-            mbar_arrive(bar(L::kSEmpty));
-            // P^T[kr][q] = exp2(s * alpha*log2e - LSE_q*log2e); causal: 0 where q < key
-            const bool diag = CAUSAL && (qt == kt);
+            ok = mbar_wait(bar(L::kSFull), cur, p.status) && mbar_wait(bar(L::kQFull + s), u & 1u, p.status);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float4* nl4 = reinterpret_cast<const float4*>(smem + L::kLse + s * 512) + c0 / 4;
+            const float4* nd4 = reinterpret_cast<const float4*>(smem + L::kDelta + s * 512) + c0 / 4;
+            float pr[64];
+            {
+                uint32_t r[2][32];
+                tmem_ld32(tmem + lane_off + L::kColS + c0, r[0]);
+                tmem_ld32(tmem + lane_off + L::kColS + c0 + 32, r[1]);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(L::kSEmpty));
+                // P^T[kr][q] = exp2(s * alpha*log2e - LSE_q*log2e)
 #pragma unroll
-            for (int c = 0; c < kBlockM; ++c) {
-                const float x = fmaf(pr[c], sl2, -lse2[c]);
-                pr[c] = (diag && c < kr) ? 0.f : ex2_approx(x);
+                for (int g = 0; g < 16; ++g) {
+                    const float4 n = nl4[g];
+                    const uint32_t* rr = &r[g >> 3][(g & 7) * 4];
+                    float x0, x1, x2, x3;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[0]), __uint_as_float(rr[1])), sl2x2, f2_pack(n.x, n.y)),
+                              x0, x1);
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2]), __uint_as_float(rr[3])), sl2x2, f2_pack(n.z, n.w)),
+                              x2, x3);
+                    pr[4 * g] = ex2_approx(x0);
+                    pr[4 * g + 1] = ex2_approx(x1);
+                    pr[4 * g + 2] = ex2_approx(x2);
+                    pr[4 * g + 3] = ex2_approx(x3);
+                }
+            }
+            if (CAUSAL && qt == kt) {
+                // diagonal tile: query q sees key kr only if q >= kr
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c0 + c < kr) pr[c] = 0.f;
             }
             if (it >= 1) {
                 ok = mbar_wait(bar(L::kPDSFree), static_cast<uint32_t>(it - 1) & 1u, p.status);
                 if (!ok) break;
             }
+            const uint32_t pt_blk = sb + L::kPt + wg * 16384;
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
+            for (int ch = 0; ch < 8; ++ch) {
                 const int c = ch * 8;
-                st_shared_v4(sb + L::kPt + (ch >> 3) * 16384 + sw128_off(kr, ch & 7), pack_bf16x2(pr[c], pr[c + 1]),
-                             pack_bf16x2(pr[c + 2], pr[c + 3]), pack_bf16x2(pr[c + 4], pr[c + 5]),
-                             pack_bf16x2(pr[c + 6], pr[c + 7]));
+                st_shared_v4(pt_blk + sw128_off(kr, ch), pack_bf16x2(pr[c], pr[c + 1]), pack_bf16x2(pr[c + 2], pr[c + 3]),
+                             pack_bf16x2(pr[c + 4], pr[c + 5]), pack_bf16x2(pr[c + 6], pr[c + 7]));
             }
             fence_async_smem();
             mbar_arrive(bar(L::kPFull));
-            // dS^T[kr][q] = alpha * P (dP - delta_q)
+            if (!L::kDQAliasS && it >= 1) {
+                // the previous tile's dQ has been computed meanwhile
+                ok = drain_dq(it - 1);
+                if (!ok) break;
+            }
+            // dS^T[kr][q] = P * (alpha * dP + (-alpha * delta_q))
             ok = mbar_wait(bar(L::kDPFull), cur, p.status);
-            if (!ok) break;
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
+            const uint32_t ds_blk = sb + L::kDSt + wg * 16384;
 #pragma unroll
-            for (int c = 0; c < kBlockM / 32; ++c) {
+            for (int h = 0; h < 2; ++h) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kColDP + c * 32, r);
+                tmem_ld32(tmem + lane_off + L::kColDP + c0 + h * 32, r);
                 tmem_wait_ld();
-                if (c == kBlockM / 32 - 1) {
+                if (h == 1) {
                     tc_fence_before();
                     mbar_arrive(bar(L::kDPEmpty));
                 }
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int q = c * 32 + h * 8;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float d0 = p.scale * pr[q + 2 * e] * (__uint_as_float(r[h * 8 + 2 * e]) - dlt[q + 2 * e]);
-                        const float d1 =
-                            p.scale * pr[q + 2 * e + 1] * (__uint_as_float(r[h * 8 + 2 * e + 1]) - dlt[q + 2 * e + 1]);
-                        w[e] = pack_bf16x2(d0, d1);
-                    }
-                    const int ch = q >> 3;
-                    st_shared_v4(sb + L::kDSt + (ch >> 3) * 16384 + sw128_off(kr, ch & 7), w[0], w[1], w[2], w[3]);
+                for (int g = 0; g < 4; ++g) {  // 8 queries per group
+                    const int c = h * 32 + g * 8;
+                    const float4 na = nd4[c / 4];
+                    const float4 nb = nd4[c / 4 + 1];
+                    const uint32_t* rr = &r[g * 8];
+                    float d[8];
+                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[0]), __uint_as_float(rr[1])), alx2, f2_pack(na.x, na.y)),
+                                     f2_pack(pr[c], pr[c + 1])), d[0], d[1]);
+                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[2]), __uint_as_float(rr[3])), alx2, f2_pack(na.z, na.w)),
+                                     f2_pack(pr[c + 2], pr[c + 3])), d[2], d[3]);
+                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[4]), __uint_as_float(rr[5])), alx2, f2_pack(nb.x, nb.y)),
+                                     f2_pack(pr[c + 4], pr[c + 5])), d[4], d[5]);
+                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[6]), __uint_as_float(rr[7])), alx2, f2_pack(nb.z, nb.w)),
+                                     f2_pack(pr[c + 6], pr[c + 7])), d[6], d[7]);
+                    st_shared_v4(ds_blk + sw128_off(kr, c >> 3), pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
+                                 pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
                 }
             }
             fence_async_smem();
             mbar_arrive(bar(L::kDSFull));
         }
-        // dK, dV epilogue
+        if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
+        if (lane == 0) bulk_wait0();
+        // dK, dV epilogue: key rows, this warpgroup's half of the d columns
         if (ok) ok = mbar_wait(bar(L::kDKVDone), 0, p.status);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
@@ -406,14 +510,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk);
-                const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
+                const uint32_t col = (which == 0 ? L::kColDV : L::kColDK) + wg * (D / 2);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tmem + lane_off + col + c * 32, r);
                     tmem_wait_ld();
                     if (!store) continue;
-                    uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + krow) * D + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + krow) * D + wg * (D / 2) +
+                                                          c * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint4 w;
@@ -426,50 +531,6 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
         }
-    } else {
-        // --------------------------------------- dQ drain (warps 4-7, query rows)
-        // Each warp owns 32 query rows and two 4 KB staging buffers; it adds
-        // its 32 x 32 FP32 slices into the workspace with its own TMA
-        // reduce-adds, so only intra-warp synchronisation is needed.
-        const int wl = warp - 4;
-        const int qr = threadIdx.x - 128;       // query row within the tile == TMEM lane
-        const int rl = lane;                    // row within this warp's box
-        const uint32_t lane_off = static_cast<uint32_t>(wl * 32) << 16;
-        const uint32_t stage0 = sb + L::kStage + wl * 2 * 4096;
-        bool ok = true;
-        int nstage = 0;
-        for (int it = 0; it < n_iter; ++it) {
-            ok = mbar_wait(bar(L::kDQFull), static_cast<uint32_t>(it) & 1u, p.status);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            const int q0 = (qt_begin + it) * kBlockM;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kColDQ + c * 32, r);
-                tmem_wait_ld();
-                if (c == D / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(L::kDQEmpty));
-                }
-                const uint32_t st = stage0 + (nstage & 1) * 4096;
-                // the reduce that last read this buffer must be done reading it
-                if (lane == 0) bulk_wait_read_le1();
-                __syncwarp();
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    st_shared_v4(st + sw128_off(rl, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2], r[4 * ch + 3]);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_3d(&tm_dqacc, st, c * 32, q0 + wl * 32, bh);
-                    bulk_commit();
-                }
-                ++nstage;
-            }
-        }
-        if (lane == 0) bulk_wait0();
-        (void)qr;
     }
 
     tc_fence_before();

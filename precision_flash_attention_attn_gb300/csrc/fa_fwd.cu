@@ -282,13 +282,26 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     if (c > lim) s[c] = -INFINITY;
             }
-            float tm = s[0];
+            // row max and tie count as 8-way trees (short dependency chains)
+            float tm;
+            {
+                float mx[8];
 #pragma unroll
-            for (int c = 1; c < kBlockN; ++c) tm = fmaxf(tm, s[c]);
+                for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+                for (int c = 8; c < kBlockN; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
+                tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            }
             if (MODE == 1 || STATS) {
-                int tc = 0;
+                int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) tc += (s[c] == tm) ? 1 : 0;
+                for (int c = 0; c < kBlockN; c += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
+                const int tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
                 if (tm > M) {
                     M = tm;
                     C = tc;
@@ -314,7 +327,7 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                 ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
                 if (!ok) break;
             }
-            float lsum = 0.f;
+            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
             int cnt = 0;
 #pragma unroll
             for (int ch = 0; ch < kBlockN / 8; ++ch) {
@@ -323,7 +336,8 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                 for (int e = 0; e < 4; ++e) {
                     const float p0 = ex2_approx(fmaf(s[ch * 8 + 2 * e], sl2, -mc_new));
                     const float p1 = ex2_approx(fmaf(s[ch * 8 + 2 * e + 1], sl2, -mc_new));
-                    lsum += p0 + p1;
+                    ls[2 * e] += p0;
+                    ls[2 * e + 1] += p1;
                     w[e] = pack_bf16x2(p0, p1);
                     if (MODE == 2) {
                         // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
@@ -338,6 +352,7 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                 st_shared_v4(p_sm + off, w[0], w[1], w[2], w[3]);
                 if (MODE == 2) st_shared_v4(plo_sm + off, wl[0], wl[1], wl[2], wl[3]);
             }
+            const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             l = l * rsc + lsum;
             if (STATS) {
                 if (changed) ones1 = 0;
