@@ -97,6 +97,36 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            fa_stream_t stream);
 
 /*
+ * fa_bwd_noalloc -- the same backward as fa_bwd, for callers that must not
+ * allocate device memory: code that runs after a framework's caching
+ * allocator has reserved (nearly) all of the GPU's memory, so a driver
+ * allocation would fail or fragment it; latency-critical loops where an
+ * allocation call may block or synchronise; deployments that forbid
+ * allocation after start-up; and devices or setups without stream-ordered
+ * memory pools.  (The paper has no counterpart; this is a deployment variant
+ * of fa_bwd.)
+ *
+ * Instead of a cudaMallocAsync workspace it uses a fixed scratch array
+ * compiled into this library, FA_NOALLOC_SCRATCH_BYTES (32 MiB) per device;
+ * every GPU that loads the library holds that array until the process exits.
+ * The caller still passes all inputs and outputs.  The call needs
+ * B*H*N*d*4 + 2*B*H*ceil(N/128)*128*4 bytes of scratch; larger problems are
+ * rejected with FA_ERR_INVALID_ARG before anything is enqueued (fa_last_error
+ * says why).  The first call on a device also looks up the array's device
+ * address on that device; make that first call before any stream capture.
+ * All calls share the one array and it keeps the previous call's contents
+ * (the backward's first kernel clears what must start at zero), so calls
+ * whose execution overlaps on the GPU -- e.g. on two streams without an
+ * ordering between them -- race on the scratch and give wrong results:
+ * serialise them.  Allocates nothing and calls no allocating routine.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, int causal, float scale, int mode,
+                   fa_stream_t stream);
+
+/*
  * fa_tie_stats -- per-row diagnostics of the forward of `mode`:
  *   tie_count[r] : number of visible keys whose FP32 raw score q.k equals the
  *                  row maximum exactly (the rs of section 3.4.5 with eps = 0);

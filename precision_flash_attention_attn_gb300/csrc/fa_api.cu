@@ -241,6 +241,103 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     return rc;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward: the workspace is a file-scope device array.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch array on the current device.  In host code
+// g_noalloc_scratch names a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress, once per device, with that device current.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail("cudaGetSymbolAddress(scratch)", e);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
+                   fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    const int BH = B * H;
+    const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
+    const size_t acc_bytes = static_cast<size_t>(BH) * N * d * sizeof(float);
+    const size_t row_bytes = static_cast<size_t>(BH) * Npad * sizeof(float);
+    const size_t ws_bytes = acc_bytes + 2 * row_bytes;
+    if (ws_bytes > FA_NOALLOC_SCRATCH_BYTES) {
+        char msg[160];
+        snprintf(msg, sizeof msg, "needs %zu bytes of scratch, the static limit is %u bytes", ws_bytes,
+                 FA_NOALLOC_SCRATCH_BYTES);
+        fa::set_error_msg("fa_bwd_noalloc", msg);
+        return FA_ERR_INVALID_ARG;
+    }
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    void* ws = nullptr;
+    if ((rc = noalloc_scratch(&ws))) return rc;
+    float* dq_acc = static_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
+    float* delta = lse2 + static_cast<size_t>(BH) * Npad;
+
+    CUtensorMap mq, mk, mv, mdo, macc;
+    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32))
+        return FA_ERR_CUDA;
+    fa::BwdArgs a{};
+    a.tm_q = &mq;
+    a.tm_k = &mk;
+    a.tm_v = &mv;
+    a.tm_do = &mdo;
+    a.tm_dqacc = &macc;
+    a.o = o;
+    a.lse = lse;
+    a.dout = dO;
+    a.dq_acc = dq_acc;
+    a.lse2 = lse2;
+    a.delta = delta;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.BH = BH;
+    a.N = N;
+    a.Npad = Npad;
+    a.d = d;
+    a.causal = causal;
+    a.mode = mode;
+    a.scale = scale;
+    a.scale_log2 = log2e_times(scale);
+    a.status = di->status;
+    return fa::launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
                  int causal, float scale, int mode, int32_t* tie_count, float* pv_err, int32_t* p_one,
                  fa_stream_t stream) {

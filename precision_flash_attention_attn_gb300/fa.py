@@ -31,6 +31,8 @@ _f = ctypes.c_float
 
 _lib.fa_fwd.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
 _lib.fa_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
+_lib.fa_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
+_lib.fa_bwd_noalloc.restype = ctypes.c_int
 _lib.fa_tie_stats.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
@@ -103,6 +105,19 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, str
     rc = _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
                      _ptr(dv), B, H, N, d, int(causal), float(scale), int(mode), _stream(stream))
     return _check("fa_bwd", rc) if check else rc
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream=None,
+                   check=True):
+    """fa_bwd with its workspace in the library's static scratch array
+    (FA_NOALLOC_SCRATCH_BYTES per device) instead of a device allocation, for
+    callers that must not allocate; overlapping calls race on the scratch."""
+    rc = _lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                             _ptr(dv), B, H, N, d, int(causal), float(scale), int(mode), _stream(stream))
+    return _check("fa_bwd_noalloc", rc) if check else rc
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err, p_one=None,
