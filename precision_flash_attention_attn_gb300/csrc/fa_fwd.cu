@@ -18,14 +18,15 @@
 //              the row max and tie count, updates the shift, waits for the
 //              previous Pbar V product, rescales the O accumulator in TMEM
 //              when the shift changed, exponentiates (ex2) while writing BF16
-//              Pbar to swizzled shared memory, and finally normalises and
-//              stores O and the LSE.
+//              Pbar to tensor memory, and finally normalises and stores O and
+//              the LSE.
 //   warp 4*NQ  TMA producer: the Q tiles once, then K and V tiles in a ring.
 //   warp 4*NQ+1  MMA issuer: S_t = Q_t K_j^T into tile t's TMEM S buffer,
-//              then O_t += Pbar_t V_j (tcgen05.mma kind::f16, A and B from
-//              shared memory).  With two query tiles the two softmax
+//              then O_t += Pbar_t V_j (tcgen05.mma kind::f16; Q, K, V from
+//              shared memory, Pbar from tensor memory).  With two query tiles the two softmax
 //              warpgroups overlap each other's MMAs and share every K/V tile.
-// TMEM columns: S_t at 128*t, O_t at 128*NQ + d*t.
+// TMEM columns: S_t at 128*t, O_t at 128*NQ + d*t, Pbar_t (BF16 pairs) after
+// the O accumulators, 64 columns each.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -37,15 +38,18 @@ namespace {
 template <int D, int MODE, int NQ>
 struct FwdLayout {
     static constexpr int kTileBytes = kBlockM * D * 2;  // 128 rows x D BF16
-    static constexpr int kStages = (D == 64) ? ((NQ == 2 && MODE == 2) ? 2 : 3) : 2;
     static constexpr int kPBytes = kBlockM * kBlockN * 2;
+    // Pbar lives in TMEM (the A operand of Pbar V).  The FP32-output mode also
+    // feeds a lo part (Pbar = hi + lo, both BF16): in TMEM where columns allow,
+    // otherwise in shared memory.
+    static constexpr bool kLoInTmem = (MODE == 2) && (NQ * (128 + D + 64 + 64) <= 512);
+    static constexpr bool kLoInSmem = (MODE == 2) && !kLoInTmem;
+    static constexpr int kStages = (D == 64) ? (kLoInSmem ? 3 : 4) : 3;
     static constexpr int kQ = 0;                                  // [NQ]
     static constexpr int kK = kQ + NQ * kTileBytes;               // [kStages]
     static constexpr int kV = kK + kStages * kTileBytes;          // [kStages]
-    static constexpr int kP = kV + kStages * kTileBytes;          // [NQ]
-    // FP32-output mode feeds Pbar to the tensor core as hi + lo BF16 parts
-    static constexpr int kPLo = kP + NQ * kPBytes;                // [NQ], mode 2
-    static constexpr int kBar = kPLo + (MODE == 2 ? NQ * kPBytes : 0);
+    static constexpr int kPLo = kV + kStages * kTileBytes;        // [NQ], mode 2 without TMEM room
+    static constexpr int kBar = kPLo + (kLoInSmem ? NQ * kPBytes : 0);
     // barriers
     static constexpr int kQFull = 0;
     static constexpr int kKFull = 1;
@@ -60,10 +64,13 @@ struct FwdLayout {
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
-    static constexpr uint32_t kTmemUsed = NQ * (128 + D);
+    static constexpr uint32_t kTmemUsed = NQ * (128 + D + 64) + (kLoInTmem ? NQ * 64 : 0);
     static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
-    static constexpr uint32_t kSCol = 0;
-    static constexpr uint32_t kOCol = 128 * NQ;
+    static_assert(kTmemUsed <= 512, "TMEM budget");
+    static constexpr uint32_t kSCol = 0;                   // [NQ] x 128: S (FP32)
+    static constexpr uint32_t kOCol = 128 * NQ;            // [NQ] x D: O accumulator
+    static constexpr uint32_t kPCol = kOCol + NQ * D;      // [NQ] x 64: Pbar (BF16 pairs)
+    static constexpr uint32_t kPLoCol = kPCol + NQ * 64;   // [NQ] x 64: Pbar lo (mode 2, if room)
     static constexpr int kThreads = 128 * NQ + 64;
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
@@ -189,14 +196,19 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                     if (!ok) return;
                     tc_fence_after();
                     const uint32_t o_t = tmem + L::kOCol + t * D;
+                    // A = Pbar from TMEM: 16 keys (8 columns) per MMA step
 #pragma unroll
                     for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t a =
-                            sdesc_sw128(sb + L::kP + t * L::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                         const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                        mma_bf16_ss(o_t, a, b, kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16_ts(o_t, tmem + L::kPCol + t * 64 + kk * 8, b, kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if (MODE == 2) {
+                    if (L::kLoInTmem) {
+#pragma unroll
+                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                            const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
+                            mma_bf16_ts(o_t, tmem + L::kPLoCol + t * 64 + kk * 8, b, kIdPV, 1u);
+                        }
+                    } else if (L::kLoInSmem) {
 #pragma unroll
                         for (int kk = 0; kk < kBlockN / 16; ++kk) {
                             const uint64_t a = sdesc_sw128(
@@ -246,7 +258,8 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + L::kSCol + t * 128;
         const uint32_t o_tm = tmem + lane_off + L::kOCol + t * D;
-        const uint32_t p_sm = sb + L::kP + t * L::kPBytes;
+        const uint32_t p_tm = tmem + lane_off + L::kPCol + t * 64;
+        const uint32_t plo_tm = tmem + lane_off + L::kPLoCol + t * 64;
         const uint32_t plo_sm = sb + L::kPLo + t * L::kPBytes;
         const float sl2 = p.scale_log2;
         float M = -INFINITY;  // running max of raw scores
@@ -282,26 +295,31 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     if (c > lim) s[c] = -INFINITY;
             }
-            // row max and tie count as 8-way trees (short dependency chains)
+            // row max: 3-input max instructions in 8 independent chains
             float tm;
             {
                 float mx[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = s[e];
+                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
 #pragma unroll
-                for (int c = 8; c < kBlockN; c += 8)
+                for (int c = 16; c < kBlockN; c += 16)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], s[c + e]);
-                tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], s[c + e], s[c + 8 + e]);
+                tm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             }
             if (MODE == 1 || STATS) {
-                int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                // The tile's tie count matters only where the tile max reaches
+                // the running max; warps where no row does skip the count (the
+                // common case once the max has settled).
+                int tc = 0;
+                if (__any_sync(0xffffffffu, tm >= M)) {
+                    int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-                for (int c = 0; c < kBlockN; c += 8)
+                    for (int c = 0; c < kBlockN; c += 8)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
-                const int tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
+                        for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
+                    tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
+                }
                 if (tm > M) {
                     M = tm;
                     C = tc;
@@ -321,23 +339,30 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
             const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
             m = m_new;
             mc = mc_new;
-            // Pbar_j may overwrite the shared P buffer and O may be rescaled
+            // Pbar_j may overwrite the TMEM Pbar buffer and O may be rescaled
             // only after O += Pbar_{j-1} V_{j-1} has completed.
             if (j >= 1) {
                 ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
                 if (!ok) break;
             }
-            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
+            // Pbar = exp2(s * alpha*log2e - m * alpha*log2e) with paired FP32 FMAs
+            // and adds; four quarters of 32 keys are packed to BF16 pairs and
+            // stored as 16 TMEM columns each (plus the lo part in mode 2)
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t nmc2 = f2_pack(-mc_new, -mc_new);
+            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 partial row sums, as 4 pairs
             int cnt = 0;
 #pragma unroll
-            for (int ch = 0; ch < kBlockN / 8; ++ch) {
-                uint32_t w[4], wl[4];
+            for (int h = 0; h < 4; ++h) {
+                uint32_t w[16], wl[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[ch * 8 + 2 * e], sl2, -mc_new));
-                    const float p1 = ex2_approx(fmaf(s[ch * 8 + 2 * e + 1], sl2, -mc_new));
-                    ls[2 * e] += p0;
-                    ls[2 * e + 1] += p1;
+                for (int e = 0; e < 16; ++e) {
+                    const int c = h * 32 + 2 * e;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nmc2), x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
                     w[e] = pack_bf16x2(p0, p1);
                     if (MODE == 2) {
                         // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
@@ -348,11 +373,23 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                     if (STATS)
                         cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
                 }
-                const uint32_t off = (ch >> 3) * 16384 + sw128_off(row, ch & 7);
-                st_shared_v4(p_sm + off, w[0], w[1], w[2], w[3]);
-                if (MODE == 2) st_shared_v4(plo_sm + off, wl[0], wl[1], wl[2], wl[3]);
+                tmem_st16(p_tm + 16 * h, w);
+                if (L::kLoInTmem) tmem_st16(plo_tm + 16 * h, wl);
+                if (L::kLoInSmem) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int ch = (h & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
+                        st_shared_v4(plo_sm + (h >> 1) * 16384 + sw128_off(row, ch), wl[4 * q], wl[4 * q + 1],
+                                     wl[4 * q + 2], wl[4 * q + 3]);
+                    }
+                }
             }
-            const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            float lsum;
+            {
+                float a0, a1;
+                f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), a0, a1);
+                lsum = a0 + a1;
+            }
             l = l * rsc + lsum;
             if (STATS) {
                 if (changed) ones1 = 0;
@@ -371,9 +408,9 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
                     tmem_st32(o_tm + c * 32, r);
                 }
-                tmem_wait_st();
             }
-            fence_async_smem();
+            tmem_wait_st();  // Pbar (and any rescaled O) written to TMEM
+            if (L::kLoInSmem) fence_async_smem();
             tc_fence_before();
             mbar_arrive(bar(L::kPFull + t));
         }
