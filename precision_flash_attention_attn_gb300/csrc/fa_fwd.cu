@@ -339,48 +339,47 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
             const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
             m = m_new;
             mc = mc_new;
+            // Pbar = exp2(s * alpha*log2e - m * alpha*log2e) with paired FP32 FMAs
+            // and adds, packed to BF16 pairs in registers (plus the lo part in
+            // mode 2).  This overlaps the previous tile's Pbar V on the tensor
+            // core; only the stores below wait for it.
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t nmc2 = f2_pack(-mc_new, -mc_new);
+            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 partial row sums, as 4 pairs
+            int cnt = 0;
+            uint32_t w[kBlockN / 2], wl[kBlockN / 2];  // wl unused (and eliminated) unless MODE == 2
+#pragma unroll
+            for (int e = 0; e < kBlockN / 2; ++e) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), sl2x2, nmc2), x0, x1);
+                const float p0 = ex2_approx(x0);
+                const float p1 = ex2_approx(x1);
+                ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
+                w[e] = pack_bf16x2(p0, p1);
+                if (MODE == 2) {
+                    // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
+                    const float h0 = __uint_as_float(w[e] << 16);
+                    const float h1 = __uint_as_float(w[e] & 0xFFFF0000u);
+                    wl[e] = pack_bf16x2(p0 - h0, p1 - h1);
+                }
+                if (STATS) cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
+            }
             // Pbar_j may overwrite the TMEM Pbar buffer and O may be rescaled
             // only after O += Pbar_{j-1} V_{j-1} has completed.
             if (j >= 1) {
                 ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
                 if (!ok) break;
             }
-            // Pbar = exp2(s * alpha*log2e - m * alpha*log2e) with paired FP32 FMAs
-            // and adds; four quarters of 32 keys are packed to BF16 pairs and
-            // stored as 16 TMEM columns each (plus the lo part in mode 2)
-            const uint64_t sl2x2 = f2_pack(sl2, sl2);
-            const uint64_t nmc2 = f2_pack(-mc_new, -mc_new);
-            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 partial row sums, as 4 pairs
-            int cnt = 0;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                uint32_t w[16], wl[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c = h * 32 + 2 * e;
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nmc2), x0, x1);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
-                    w[e] = pack_bf16x2(p0, p1);
-                    if (MODE == 2) {
-                        // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
-                        const float h0 = __uint_as_float(w[e] << 16);
-                        const float h1 = __uint_as_float(w[e] & 0xFFFF0000u);
-                        wl[e] = pack_bf16x2(p0 - h0, p1 - h1);
-                    }
-                    if (STATS)
-                        cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
-                }
-                tmem_st16(p_tm + 16 * h, w);
-                if (L::kLoInTmem) tmem_st16(plo_tm + 16 * h, wl);
+                tmem_st16(p_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * h]));
+                if (L::kLoInTmem) tmem_st16(plo_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&wl[16 * h]));
                 if (L::kLoInSmem) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int ch = (h & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
-                        st_shared_v4(plo_sm + (h >> 1) * 16384 + sw128_off(row, ch), wl[4 * q], wl[4 * q + 1],
-                                     wl[4 * q + 2], wl[4 * q + 3]);
+                        st_shared_v4(plo_sm + (h >> 1) * 16384 + sw128_off(row, ch), wl[16 * h + 4 * q],
+                                     wl[16 * h + 4 * q + 1], wl[16 * h + 4 * q + 2], wl[16 * h + 4 * q + 3]);
                     }
                 }
             }
