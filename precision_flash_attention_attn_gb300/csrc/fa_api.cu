@@ -28,6 +28,7 @@ struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int* status = nullptr;
+    int num_sms = 0;
 };
 
 std::mutex g_mu;
@@ -53,6 +54,9 @@ int device_info(DeviceInfo** out) {
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return FA_ERR_CUDA;
         di.supported = (major == 10 && minor == 3);
+        if (di.supported &&
+            cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
         if (di.supported) {
             void* p = nullptr;
             ce = cudaGetSymbolAddress(&p, g_fa_status);
@@ -149,15 +153,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
+    // O as a TMA store target: 64 BF16 or 32 FP32 columns (128 bytes) per box row
+    const bool o32 = (mode == 2);
     if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mo, o, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o32 ? 4 : 2, BH, N,
+                 d, o32 ? 32 : 64))
         return FA_ERR_CUDA;
     fa::FwdArgs a{};
     a.tm_q = &mq;
     a.tm_k = &mk;
     a.tm_v = &mv;
+    a.tm_o = &mo;
     a.o = o;
     a.lse = lse;
     a.BH = BH;
@@ -168,6 +177,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.scale = scale;
     a.scale_log2 = log2e_times(scale);
     a.status = di->status;
+    a.num_sms = di->num_sms;
     return fa::launch_fwd(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -234,6 +244,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         a.scale = scale;
         a.scale_log2 = log2e_times(scale);
         a.status = di->status;
+        a.num_sms = di->num_sms;
         if (fa::launch_bwd(a, st) != cudaSuccess) rc = FA_ERR_CUDA;
     }
     const cudaError_t fe = cudaFreeAsync(ws, st);
@@ -335,6 +346,7 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
     a.scale = scale;
     a.scale_log2 = log2e_times(scale);
     a.status = di->status;
+    a.num_sms = di->num_sms;
     return fa::launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -359,6 +371,7 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int
     a.tm_q = &mq;
     a.tm_k = &mk;
     a.tm_v = &mv;
+    a.tm_o = &mq;  // not read: the statistics variant writes no O
     a.o = nullptr;
     a.lse = nullptr;
     a.tie_count = tie_count;
@@ -371,6 +384,7 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int
     a.scale = scale;
     a.scale_log2 = log2e_times(scale);
     a.status = di->status;
+    a.num_sms = di->num_sms;
     if (fa::launch_fwd(a, true, st) != cudaSuccess) return FA_ERR_CUDA;
     fa::StatsArgs s{};
     s.q = q;

@@ -21,10 +21,16 @@
 //              Pbar to tensor memory, and finally normalises and stores O and
 //              the LSE.
 //   warp 4*NQ  TMA producer: the Q tiles once, then K and V tiles in a ring.
-//   warp 4*NQ+1  MMA issuer: S_t = Q_t K_j^T into tile t's TMEM S buffer,
-//              then O_t += Pbar_t V_j (tcgen05.mma kind::f16; Q, K, V from
-//              shared memory, Pbar from tensor memory).  With two query tiles the two softmax
-//              warpgroups overlap each other's MMAs and share every K/V tile.
+//   warp 4*NQ+1+t  MMA issuer of query tile t: S_t = Q_t K_j^T into the
+//              tile's TMEM S buffer as soon as the softmax has read the
+//              previous S, then O_t += Pbar_t V_{j-1} (tcgen05.mma kind::f16;
+//              Q, K, V from shared memory, Pbar from tensor memory).  One
+//              issuer per tile keeps the two tiles' chains independent: each
+//              softmax warpgroup waits only for its own MMAs, and the tensor
+//              core interleaves the two tiles' work.  A K/V stage is refilled
+//              once every tile that reads it has finished its PV product.
+// With two query tiles the CTA has three warpgroups; the producer/MMA
+// warpgroup hands registers to the two softmax warpgroups (setmaxnreg).
 // TMEM columns: S_t at 128*t, O_t at 128*NQ + d*t, Pbar_t (BF16 pairs) after
 // the O accumulators, 64 columns each.
 #include <cuda_bf16.h>
@@ -44,23 +50,39 @@ struct FwdLayout {
     // otherwise in shared memory.
     static constexpr bool kLoInTmem = (MODE == 2) && (NQ * (128 + D + 64 + 64) <= 512);
     static constexpr bool kLoInSmem = (MODE == 2) && !kLoInTmem;
+    // Q is double-buffered where shared memory allows, so the next work
+    // item's Q lands while the current one is still being multiplied.
+    static constexpr int kQBufs = (D == 64) ? 2 : 1;
     static constexpr int kStages = (D == 64) ? (kLoInSmem ? 3 : 4) : 3;
-    static constexpr int kQ = 0;                                  // [NQ]
-    static constexpr int kK = kQ + NQ * kTileBytes;               // [kStages]
+    static constexpr int kQ = 0;                                  // [kQBufs][NQ]
+    static constexpr int kK = kQ + kQBufs * NQ * kTileBytes;      // [kStages]
     static constexpr int kV = kK + kStages * kTileBytes;          // [kStages]
     static constexpr int kPLo = kV + kStages * kTileBytes;        // [NQ], mode 2 without TMEM room
-    static constexpr int kBar = kPLo + (kLoInSmem ? NQ * kPBytes : 0);
+    // With d = 64 the epilogue stages O in shared memory and writes it with
+    // TMA stores (row-per-thread global stores would scatter 32 rows per
+    // warp instruction).  The FP32-output mode stages O in its lo buffer,
+    // which is free between the item's last Pbar V and the next item's first
+    // Pbar; the other modes have a buffer of their own.
+    static constexpr bool kTmaStoreO = (D == 64);
+    static constexpr int kOStageBytes = kBlockM * D * 2;
+    static constexpr int kOStage = kPLo + (kLoInSmem ? NQ * kPBytes : 0);  // [NQ], modes 0 and 1
+    static constexpr int kBar = kOStage + ((kTmaStoreO && MODE != 2) ? NQ * kOStageBytes : 0);
+    static_assert(!kTmaStoreO || MODE != 2 || kLoInSmem, "FP32 O staging uses the lo buffer");
     // barriers
-    static constexpr int kQFull = 0;
-    static constexpr int kKFull = 1;
-    static constexpr int kVFull = kKFull + kStages;
-    static constexpr int kKVEmpty = kVFull + kStages;
-    static constexpr int kSFull = kKVEmpty + kStages;  // [NQ]
+    static constexpr int kQFull = 0;                     // [kQBufs]
+    static constexpr int kQEmpty = kQFull + kQBufs;      // [kQBufs], one arrival per tile
+    static constexpr int kKFull = kQEmpty + kQBufs;      // [kStages]
+    static constexpr int kVFull = kKFull + kStages;      // [kStages]
+    static constexpr int kKVEmpty = kVFull + kStages;    // [NQ][kStages]
+    static constexpr int kSFull = kKVEmpty + NQ * kStages;  // [NQ]
     static constexpr int kSEmpty = kSFull + NQ;        // [NQ]
     static constexpr int kPFull = kSEmpty + NQ;        // [NQ]
     static constexpr int kODone = kPFull + NQ;         // [NQ]
-    static constexpr int kDrain = kODone + NQ;
-    static constexpr int kNumBars = kDrain + 1;
+    static constexpr int kOFree = kODone + NQ;         // [NQ]: O read out by the epilogue
+    static constexpr int kOStaged = kOFree + NQ;       // [NQ]: O rows written to the staging buffer
+    static constexpr int kStageFree = kOStaged + NQ;   // [NQ]: previous TMA store has read the buffer
+    static constexpr int kDrain = kStageFree + NQ;     // [NQ]
+    static constexpr int kNumBars = kDrain + NQ;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -71,7 +93,14 @@ struct FwdLayout {
     static constexpr uint32_t kOCol = 128 * NQ;            // [NQ] x D: O accumulator
     static constexpr uint32_t kPCol = kOCol + NQ * D;      // [NQ] x 64: Pbar (BF16 pairs)
     static constexpr uint32_t kPLoCol = kPCol + NQ * 64;   // [NQ] x 64: Pbar lo (mode 2, if room)
-    static constexpr int kThreads = 128 * NQ + 64;
+    // softmax warpgroups, then producer + one MMA warp per tile (padded to a
+    // whole warpgroup when registers are rebalanced)
+    static constexpr int kThreads = NQ == 2 ? 384 : 192;
+    // register budgets with two tiles (2 x 128 x softmax + 128 x other =
+    // 384 x 168): the FP32-output mode's MMA warps issue the lo products too
+    static constexpr uint32_t kRegsSoftmax = MODE == 2 ? 200 : 216;
+    static constexpr uint32_t kRegsOther = MODE == 2 ? 104 : 72;
+    static_assert(NQ != 2 || 256 * kRegsSoftmax + 128 * kRegsOther == 384 * 168, "register split");
     static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -81,18 +110,33 @@ struct FwdParams {
     int32_t* tie_count;
     int32_t* p_one;
     int BH, N;
+    int n_cq;     // query-tile groups (of NQ tiles) per (batch, head)
+    int n_items;  // BH * n_cq work items
     float scale_log2;
     int* status;
 };
 
+// Work items are (query-tile group, batch-head) pairs, numbered longest first
+// (largest causal group index first).  CTA c takes items in a snake order over
+// rounds of gridDim.x: round r visits c on even rounds and gridDim.x-1-c on
+// odd ones, which balances the causal work nearly as well as greedy longest-
+// processing-time scheduling.
+__device__ __forceinline__ int fwd_item(int r) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
 template <int D, int MODE, bool CAUSAL, bool STATS, int NQ>
-__global__ void __launch_bounds__(128 * NQ + 64, 1)
+__global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const FwdParams p) {
     using L = FwdLayout<D, MODE, NQ>;
     constexpr int S = L::kStages;
+    constexpr int QB = L::kQBufs;
     constexpr int kProducerWarp = 4 * NQ;
-    constexpr int kMmaWarp = 4 * NQ + 1;
+    constexpr int kMmaWarp0 = 4 * NQ + 1;  // MMA issuer of tile t: warp kMmaWarp0 + t
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -101,39 +145,47 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int cq = gridDim.y - 1 - blockIdx.y;  // longest causal tiles first
     const int n_ktiles_all = (p.N + kBlockN - 1) / kBlockN;
-    // per query tile: first row and number of key tiles it visits (0: past N)
-    int q0s[NQ], nkts[NQ];
-    int n_kt = 0, n_active = 0;
-#pragma unroll
-    for (int t = 0; t < NQ; ++t) {
+    // Work item -> (batch-head, group); per query tile t of the group: first
+    // row and number of key tiles it visits (0: the tile lies past N).
+    auto item_bh = [&](int it) { return it % p.BH; };
+    auto item_cq = [&](int it) { return p.n_cq - 1 - it / p.BH; };
+    auto tile_q0 = [&](int cq, int t) { return (cq * NQ + t) * kBlockM; };
+    auto tile_nkt = [&](int cq, int t) {
         const int qt = cq * NQ + t;
-        q0s[t] = qt * kBlockM;
-        const bool active = q0s[t] < p.N;
-        nkts[t] = !active ? 0 : (CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all);
-        n_kt = nkts[t] > n_kt ? nkts[t] : n_kt;
-        n_active += active ? 1 : 0;
-    }
+        if (qt * kBlockM >= p.N) return 0;
+        return CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all;
+    };
+    auto item_nkt = [&](int cq) {
+        int n = 0;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) n = tile_nkt(cq, t) > n ? tile_nkt(cq, t) : n;
+        return n;
+    };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kQFull), 1);
+        for (int b = 0; b < QB; ++b) {
+            mbar_init(bar(L::kQFull + b), 1);
+            mbar_init(bar(L::kQEmpty + b), NQ);
+        }
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(L::kKFull + s), 1);
             mbar_init(bar(L::kVFull + s), 1);
-            mbar_init(bar(L::kKVEmpty + s), 1);
         }
         for (int t = 0; t < NQ; ++t) {
+            for (int s = 0; s < S; ++s) mbar_init(bar(L::kKVEmpty + t * S + s), 1);
             mbar_init(bar(L::kSFull + t), 1);
             mbar_init(bar(L::kSEmpty + t), 128);
             mbar_init(bar(L::kPFull + t), 128);
             mbar_init(bar(L::kODone + t), 1);
+            mbar_init(bar(L::kOFree + t), 128);
+            mbar_init(bar(L::kOStaged + t), 128);
+            mbar_init(bar(L::kStageFree + t), 1);
+            mbar_init(bar(L::kDrain + t), 1);
         }
-        mbar_init(bar(L::kDrain), 1);
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(sb + L::kTmemSlot, L::kTmemCols);
         tmem_relinquish();
     }
@@ -142,119 +194,180 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(L::kQFull), L::kTileBytes * n_active);
-            for (int t = 0; t < NQ; ++t) {
-                if (nkts[t] == 0) continue;
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sb + L::kQ + t * L::kTileBytes + b * 16384, &tm_q, bar(L::kQFull), b * 64, q0s[t],
-                                bh);
+    if (warp >= kProducerWarp) {
+        if (NQ == 2) regs_dec<L::kRegsOther>();
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------ TMA producer
+            // Streams every item's Q tiles and K/V tiles through the rings,
+            // running ahead into the next item as far as the buffers allow.
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                bool ok = true;
+                int g = 0;  // K/V tiles issued so far (all items)
+                int n = 0;  // items started
+                for (int r = 0; ok; ++r, ++n) {
+                    const int it = fwd_item(r);
+                    if (it >= p.n_items) break;
+                    const int bh = item_bh(it), cq = item_cq(it);
+                    const int qb = n % QB;
+                    const uint32_t uq = static_cast<uint32_t>(n / QB);
+                    // the Q buffer is free once both tiles' last S of item n - QB is done
+                    if (n >= QB) ok = mbar_wait(bar(L::kQEmpty + qb), (uq - 1) & 1u, p.status);
+                    if (!ok) break;
+                    int n_active = 0;
+                    for (int t = 0; t < NQ; ++t) n_active += tile_nkt(cq, t) > 0 ? 1 : 0;
+                    mbar_arrive_expect_tx(bar(L::kQFull + qb), L::kTileBytes * n_active);
+                    for (int t = 0; t < NQ; ++t) {
+                        if (tile_nkt(cq, t) == 0) continue;
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(sb + L::kQ + (qb * NQ + t) * L::kTileBytes + b * 16384, &tm_q,
+                                        bar(L::kQFull + qb), b * 64, tile_q0(cq, t), bh);
+                    }
+                    const int n_kt = item_nkt(cq);
+                    for (int j = 0; j < n_kt; ++j, ++g) {
+                        const int s = g % S;
+                        const uint32_t u = static_cast<uint32_t>(g / S);
+                        // stage s is free once every tile has released round u-1
+                        if (g >= S)
+                            for (int t = 0; t < NQ && ok; ++t)
+                                ok = mbar_wait(bar(L::kKVEmpty + t * S + s), (u - 1) & 1u, p.status);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
+                                        b * 64, j * kBlockN, bh);
+                        mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTileBytes);
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
+                                        b * 64, j * kBlockN, bh);
+                    }
+                }
+                // Every copy this thread issued must have landed before the CTA
+                // may exit (normally long since true).
+                for (int m = n - QB > 0 ? n - QB : 0; m < n; ++m)
+                    mbar_wait(bar(L::kQFull + m % QB), static_cast<uint32_t>(m / QB) & 1u, p.status);
+                for (int h = g - S > 0 ? g - S : 0; h < g; ++h) {
+                    const uint32_t u = static_cast<uint32_t>(h / S);
+                    mbar_wait(bar(L::kKFull + h % S), u & 1u, p.status);
+                    mbar_wait(bar(L::kVFull + h % S), u & 1u, p.status);
+                }
             }
-            int issued = 0;
-            for (int j = 0; j < n_kt; ++j) {
-                const int s = j % S;
-                const uint32_t u = static_cast<uint32_t>(j / S);
-                if (j >= S && !mbar_wait(bar(L::kKVEmpty + s), (u - 1) & 1u, p.status)) break;
-                mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
-                                b * 64, j * kBlockN, bh);
-                mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTileBytes);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
-                                b * 64, j * kBlockN, bh);
-                issued = j + 1;
-            }
-            // Every copy this thread issued must have landed before the CTA
-            // may exit (normally long since true).
-            mbar_wait(bar(L::kQFull), 0, p.status);
-            for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j) {
-                const uint32_t u = static_cast<uint32_t>(j / S);
-                mbar_wait(bar(L::kKFull + j % S), u & 1u, p.status);
-                mbar_wait(bar(L::kVFull + j % S), u & 1u, p.status);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        } else if (warp < kMmaWarp0 + NQ) {
+            // ------------------------------------------ MMA issuer of query tile t
+            // The whole warp runs the loop and waits; one elected lane issues each
+            // group of MMAs together with the commits that track them.  Per item:
+            // S(0), then S(j) and Pbar V(j-1) alternately, then Pbar V(last).
+            const int t = warp - kMmaWarp0;
             constexpr uint32_t kIdS = idesc_bf16(kBlockM, kBlockN, false, false);
             constexpr uint32_t kIdPV = idesc_bf16(kBlockM, D, false, true);
-            bool ok = mbar_wait(bar(L::kQFull), 0, p.status);
-            auto issue_pv = [&](int jj) {
-                const int s = jj % S;
-                const uint32_t u = static_cast<uint32_t>(jj / S);
-                ok = ok && mbar_wait(bar(L::kVFull + s), u & 1u, p.status);
-#pragma unroll
-                for (int t = 0; t < NQ; ++t) {
-                    if (jj >= nkts[t]) continue;
-                    ok = ok && mbar_wait(bar(L::kPFull + t), static_cast<uint32_t>(jj) & 1u, p.status);
-                    if (!ok) return;
-                    tc_fence_after();
-                    const uint32_t o_t = tmem + L::kOCol + t * D;
+            const uint32_t s_acc = tmem + L::kSCol + t * 128;
+            const uint32_t o_acc = tmem + L::kOCol + t * D;
+            const uint32_t p_tm = tmem + L::kPCol + t * 64;
+            const uint32_t plo_tm = tmem + L::kPLoCol + t * 64;
+            auto wait_all = [&](uint32_t b, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
+            };
+            bool ok = true;
+            bool issued = false;
+            int g = 0;   // K/V ring position of the current item's first tile
+            int cs = 0;  // S (and Pbar) products of this tile so far, all items
+            int e = 0;   // items this tile has finished (epilogues)
+            // Pbar V for local key tile jj whose Pbar is number c of this tile
+            auto issue_pv = [&](int jj, int c) {
+                const int s = (g + jj) % S;
+                const uint32_t u = static_cast<uint32_t>((g + jj) / S);
+                ok = ok && wait_all(bar(L::kVFull + s), u & 1u);
+                ok = ok && wait_all(bar(L::kPFull + t), static_cast<uint32_t>(c) & 1u);
+                // the first product of an item overwrites O: the previous
+                // item's epilogue must have read it out
+                if (jj == 0 && e >= 1) ok = ok && wait_all(bar(L::kOFree + t), static_cast<uint32_t>(e - 1) & 1u);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t v_sm = sb + L::kV + s * L::kTileBytes;
+                if (elect_one()) {
                     // A = Pbar from TMEM: 16 keys (8 columns) per MMA step
 #pragma unroll
-                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                        const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                        mma_bf16_ts(o_t, tmem + L::kPCol + t * 64 + kk * 8, b, kIdPV, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kBlockN / 16; ++kk)
+                        mma_bf16_ts(o_acc, p_tm + kk * 8, sdesc_sw128(v_sm + kk * 2048, 16384, 1024), kIdPV,
+                                    (jj > 0 || kk > 0) ? 1u : 0u);
                     if (L::kLoInTmem) {
 #pragma unroll
-                        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                            const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                            mma_bf16_ts(o_t, tmem + L::kPLoCol + t * 64 + kk * 8, b, kIdPV, 1u);
-                        }
+                        for (int kk = 0; kk < kBlockN / 16; ++kk)
+                            mma_bf16_ts(o_acc, plo_tm + kk * 8, sdesc_sw128(v_sm + kk * 2048, 16384, 1024), kIdPV,
+                                        1u);
                     } else if (L::kLoInSmem) {
 #pragma unroll
                         for (int kk = 0; kk < kBlockN / 16; ++kk) {
                             const uint64_t a = sdesc_sw128(
                                 sb + L::kPLo + t * L::kPBytes + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                            const uint64_t b = sdesc_sw128(sb + L::kV + s * L::kTileBytes + kk * 2048, 16384, 1024);
-                            mma_bf16_ss(o_t, a, b, kIdPV, 1u);
+                            mma_bf16_ss(o_acc, a, sdesc_sw128(v_sm + kk * 2048, 16384, 1024), kIdPV, 1u);
                         }
                     }
                     mma_commit(bar(L::kODone + t));
+                    mma_commit(bar(L::kKVEmpty + t * S + s));
                 }
-                if (ok) mma_commit(bar(L::kKVEmpty + s));
+                __syncwarp();
             };
-            for (int j = 0; j < n_kt && ok; ++j) {
-                const int s = j % S;
-                const uint32_t u = static_cast<uint32_t>(j / S);
-                ok = mbar_wait(bar(L::kKFull + s), u & 1u, p.status);
-#pragma unroll
-                for (int t = 0; t < NQ; ++t) {
-                    if (!ok || j >= nkts[t]) continue;
-                    if (j >= 1)
-                        ok = mbar_wait(bar(L::kSEmpty + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
+            for (int r = 0, n = 0; ok; ++r, ++n) {
+                const int it = fwd_item(r);
+                if (it >= p.n_items) break;
+                const int cq = item_cq(it);
+                const int nkt = tile_nkt(cq, t);
+                const int n_kt = item_nkt(cq);
+                const int qb = n % QB;
+                const uint32_t q_sm = sb + L::kQ + (qb * NQ + t) * L::kTileBytes;
+                if (nkt > 0) ok = wait_all(bar(L::kQFull + qb), static_cast<uint32_t>(n / QB) & 1u);
+                for (int j = 0; j < nkt && ok; ++j) {
+                    const int s = (g + j) % S;
+                    const uint32_t u = static_cast<uint32_t>((g + j) / S);
+                    ok = wait_all(bar(L::kKFull + s), u & 1u);
+                    // S overwrites the tile's S buffer once the softmax has read the previous one
+                    if (ok && cs >= 1) ok = wait_all(bar(L::kSEmpty + t), static_cast<uint32_t>(cs - 1) & 1u);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint32_t k_sm = sb + L::kK + s * L::kTileBytes;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint64_t a = sdesc_sw128(sb + L::kQ + t * L::kTileBytes + koff, 16, 1024);
-                        const uint64_t b = sdesc_sw128(sb + L::kK + s * L::kTileBytes + koff, 16, 1024);
-                        mma_bf16_ss(tmem + L::kSCol + t * 128, a, b, kIdS, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_bf16_ss(s_acc, sdesc_sw128(q_sm + koff, 16, 1024), sdesc_sw128(k_sm + koff, 16, 1024),
+                                        kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(L::kSFull + t));
+                        if (j == nkt - 1) mma_commit(bar(L::kQEmpty + qb));  // last read of this Q tile
                     }
-                    mma_commit(bar(L::kSFull + t));
+                    __syncwarp();
+                    issued = true;
+                    ++cs;
+                    if (j >= 1) issue_pv(j - 1, cs - 2);
                 }
-                if (ok && j >= 1) issue_pv(j - 1);
+                if (ok && nkt > 0) issue_pv(nkt - 1, cs - 1);
+                if (!ok) break;
+                // Tiles and Q buffers this tile does not read are released in
+                // order behind its earlier products (a commit arrives only once
+                // everything this thread issued before it has completed).
+                if (elect_one()) {
+                    if (nkt == 0) mma_commit(bar(L::kQEmpty + qb));
+                    for (int j = nkt; j < n_kt; ++j) mma_commit(bar(L::kKVEmpty + t * S + (g + j) % S));
+                }
+                __syncwarp();
+                g += n_kt;
+                if (nkt > 0) ++e;
             }
-            if (ok && n_kt > 0) issue_pv(n_kt - 1);
-            // Drain: every MMA issued above has completed before TMEM is freed.
-            mma_commit(bar(L::kDrain));
-            mbar_wait(bar(L::kDrain), 0, p.status);
+            // Drain: every MMA this warp issued has completed before TMEM is freed.
+            if (issued) {
+                if (elect_one()) mma_commit(bar(L::kDrain + t));
+                __syncwarp();
+                mbar_wait(bar(L::kDrain + t), 0, p.status);
+            }
         }
     } else {
+        if (NQ == 2) regs_inc<L::kRegsSoftmax>();
         // ---------------------------------------------------------- softmax
         const int t = warp >> 2;               // query tile of this warpgroup
         const int row = threadIdx.x & 127;     // == TMEM lane
-        const int q0 = q0s[t];
-        const int nkt = nkts[t];
-        const int qrow = q0 + row;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + L::kSCol + t * 128;
         const uint32_t o_tm = tmem + lane_off + L::kOCol + t * D;
@@ -262,205 +375,288 @@ __global__ void __launch_bounds__(128 * NQ + 64, 1)
         const uint32_t plo_tm = tmem + lane_off + L::kPLoCol + t * 64;
         const uint32_t plo_sm = sb + L::kPLo + t * L::kPBytes;
         const float sl2 = p.scale_log2;
-        float M = -INFINITY;  // running max of raw scores
-        int C = 0;            // running count of keys equal to M
-        float m = -INFINITY;  // current shift, raw units
-        float mc = -INFINITY; // m * sl2
-        float l = 0.f;
-        int ones0 = 0, ones1 = 0;
+        // waits return the same verdict to every lane (tcgen05.ld/st below
+        // are warp-collective)
+        auto wait_w = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
+        };
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            ok = mbar_wait(bar(L::kSFull + t), static_cast<uint32_t>(j) & 1u, p.status);
+        int cs = 0;  // S products of this tile consumed so far, all items
+        int ne = 0;  // epilogues this warpgroup has finished
+        // The staging buffer may be rewritten once the previous epilogue's TMA
+        // store has read it: its issuing thread (row 0) checks and signals.
+        auto stage_free = [&]() {
+            if (row == 0) {
+                bulk_wait_read0();
+                mbar_arrive(bar(L::kStageFree + t));
+            }
+            return wait_w(bar(L::kStageFree + t), static_cast<uint32_t>(ne - 1) & 1u);
+        };
+        if (L::kTmaStoreO && t == 0 && threadIdx.x == 0) tma_prefetch_desc(&tm_o);
+        for (int r = 0; ok; ++r) {
+            const int it = fwd_item(r);
+            if (it >= p.n_items) break;
+            const int bh = item_bh(it), cq = item_cq(it);
+            const int nkt = tile_nkt(cq, t);
+            if (nkt == 0) continue;
+            const int q0 = tile_q0(cq, t);
+            const int qrow = q0 + row;
+            float M = -INFINITY;  // running max of raw scores
+            int C = 0;            // running count of keys equal to M
+            float m = -INFINITY;  // current shift, raw units
+            float mc = -INFINITY; // m * sl2
+            float l = 0.f;
+            int ones0 = 0, ones1 = 0;
+            for (int j = 0; j < nkt; ++j, ++cs) {
+                ok = wait_w(bar(L::kSFull + t), static_cast<uint32_t>(cs) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                float s[kBlockN];
+                {
+                    uint32_t rr[kBlockN / 32][32];
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(s_tm + c * 32, rr[c]);
+                    tmem_wait_ld();  // one wait for all four loads
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[c][e]);
+                }
+                tc_fence_before();
+                mbar_arrive(bar(L::kSEmpty + t));  // S is in registers: the next S may land
+
+                const int k0 = j * kBlockN;
+                const bool need_mask = CAUSAL ? (k0 + kBlockN > q0) : (k0 + kBlockN > p.N);
+                if (need_mask) {
+                    const int lim = CAUSAL ? (qrow - k0) : (p.N - 1 - k0);  // keep keys c <= lim
+#pragma unroll
+                    for (int c = 0; c < kBlockN; ++c)
+                        if (c > lim) s[c] = -INFINITY;
+                }
+                // row max: 3-input max instructions in 8 independent chains
+                float tm;
+                {
+                    float mx[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
+#pragma unroll
+                    for (int c = 16; c < kBlockN; c += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], s[c + e], s[c + 8 + e]);
+                    tm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                }
+                if (MODE == 1 || STATS) {
+                    // The tile's tie count matters only where the tile max reaches
+                    // the running max; warps where no row does skip the count (the
+                    // common case once the max has settled).
+                    int tc = 0;
+                    if (__any_sync(0xffffffffu, tm >= M)) {
+                        int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                        for (int c = 0; c < kBlockN; c += 8)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
+                        tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
+                    }
+                    if (tm > M) {
+                        M = tm;
+                        C = tc;
+                    } else if (tm == M) {
+                        C += tc;
+                    }
+                } else {
+                    M = fmaxf(M, tm);
+                }
+                float m_new = M;
+                if (MODE == 1 && C > 1) {
+                    if (M > 0.f) m_new = kStabBeta * M;
+                    else if (M < 0.f) m_new = 0.f;
+                }
+                const float mc_new = m_new * sl2;
+                const bool changed = (m_new != m);
+                const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
+                m = m_new;
+                mc = mc_new;
+                // Pbar = exp2(s * alpha*log2e - m * alpha*log2e) with paired FP32 FMAs
+                // and adds, packed to BF16 pairs in registers (plus the lo part in
+                // mode 2).  This overlaps the previous tile's Pbar V on the tensor
+                // core; only the stores below wait for it.
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+                const uint64_t nmc2 = f2_pack(-mc_new, -mc_new);
+                uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 partial row sums, as 4 pairs
+                int cnt = 0;
+                uint32_t w[kBlockN / 2], wl[kBlockN / 2];  // wl unused (and eliminated) unless MODE == 2
+#pragma unroll
+                for (int e = 0; e < kBlockN / 2; ++e) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), sl2x2, nmc2), x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
+                    w[e] = pack_bf16x2(p0, p1);
+                    if (MODE == 2) {
+                        // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
+                        const float h0 = __uint_as_float(w[e] << 16);
+                        const float h1 = __uint_as_float(w[e] & 0xFFFF0000u);
+                        wl[e] = pack_bf16x2(p0 - h0, p1 - h1);
+                    }
+                    if (STATS) cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
+                }
+                // Pbar may overwrite the TMEM Pbar buffer and O may be rescaled
+                // only after the previous Pbar V product (of this or the
+                // previous item) has completed.
+                if (cs >= 1) {
+                    ok = wait_w(bar(L::kODone + t), static_cast<uint32_t>(cs - 1) & 1u);
+                    if (!ok) break;
+                }
+                // FP32 output: the lo buffer held the previous item's O for its TMA store
+                if (L::kTmaStoreO && !STATS && L::kLoInSmem && j == 0 && ne >= 1) {
+                    ok = stage_free();
+                    if (!ok) break;
+                }
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    tmem_st16(p_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * h]));
+                    if (L::kLoInTmem) tmem_st16(plo_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&wl[16 * h]));
+                    if (L::kLoInSmem) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int ch = (h & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
+                            st_shared_v4(plo_sm + (h >> 1) * 16384 + sw128_off(row, ch), wl[16 * h + 4 * q],
+                                         wl[16 * h + 4 * q + 1], wl[16 * h + 4 * q + 2], wl[16 * h + 4 * q + 3]);
+                        }
+                    }
+                }
+                float lsum;
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), a0, a1);
+                    lsum = a0 + a1;
+                }
+                l = l * rsc + lsum;
+                if (STATS) {
+                    if (changed) ones1 = 0;
+                    ones0 += cnt;
+                    ones1 += cnt;
+                }
+                // rescale O after the scores are consumed (keeps register use low)
+                if (j >= 1 && __any_sync(0xffffffffu, changed)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_tm + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
+                        tmem_st32(o_tm + c * 32, r);
+                    }
+                }
+                tmem_wait_st();  // Pbar (and any rescaled O) written to TMEM
+                if (L::kLoInSmem) fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(L::kPFull + t));
+            }
+            if (!ok) break;
+            // ------------------------------------------------------ epilogue
+            // Read O out of TMEM (which frees it for the next item's first
+            // product), then normalise and store O and the LSE.
+            ok = wait_w(bar(L::kODone + t), static_cast<uint32_t>(cs - 1) & 1u);
             if (!ok) break;
             tc_fence_after();
-            float s[kBlockN];
-            {
-                uint32_t r[kBlockN / 32][32];
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(s_tm + c * 32, r[c]);
-                tmem_wait_ld();  // one wait for all four loads
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
-            }
-            tc_fence_before();
-            mbar_arrive(bar(L::kSEmpty + t));  // S is in registers: the next S may land
-
-            const int k0 = j * kBlockN;
-            const bool need_mask = CAUSAL ? (k0 + kBlockN > q0) : (k0 + kBlockN > p.N);
-            if (need_mask) {
-                const int lim = CAUSAL ? (qrow - k0) : (p.N - 1 - k0);  // keep keys c <= lim
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (c > lim) s[c] = -INFINITY;
-            }
-            // row max: 3-input max instructions in 8 independent chains
-            float tm;
-            {
-                float mx[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
-#pragma unroll
-                for (int c = 16; c < kBlockN; c += 16)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], s[c + e], s[c + 8 + e]);
-                tm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            }
-            if (MODE == 1 || STATS) {
-                // The tile's tie count matters only where the tile max reaches
-                // the running max; warps where no row does skip the count (the
-                // common case once the max has settled).
-                int tc = 0;
-                if (__any_sync(0xffffffffu, tm >= M)) {
-                    int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-                    for (int c = 0; c < kBlockN; c += 8)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
-                    tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
-                }
-                if (tm > M) {
-                    M = tm;
-                    C = tc;
-                } else if (tm == M) {
-                    C += tc;
+            const bool store = qrow < p.N;
+            const size_t rowid = static_cast<size_t>(bh) * p.N + qrow;
+            if (STATS) {
+                tc_fence_before();
+                mbar_arrive(bar(L::kOFree + t));
+                if (store) {
+                    p.tie_count[rowid] = C;
+                    if (p.p_one) {
+                        p.p_one[rowid] = ones0;
+                        p.p_one[static_cast<size_t>(p.BH) * p.N + rowid] = ones1;
+                    }
                 }
             } else {
-                M = fmaxf(M, tm);
-            }
-            float m_new = M;
-            if (MODE == 1 && C > 1) {
-                if (M > 0.f) m_new = kStabBeta * M;
-                else if (M < 0.f) m_new = 0.f;
-            }
-            const float mc_new = m_new * sl2;
-            const bool changed = (m_new != m);
-            const float rsc = changed ? ex2_approx(mc - mc_new) : 1.f;
-            m = m_new;
-            mc = mc_new;
-            // Pbar = exp2(s * alpha*log2e - m * alpha*log2e) with paired FP32 FMAs
-            // and adds, packed to BF16 pairs in registers (plus the lo part in
-            // mode 2).  This overlaps the previous tile's Pbar V on the tensor
-            // core; only the stores below wait for it.
-            const uint64_t sl2x2 = f2_pack(sl2, sl2);
-            const uint64_t nmc2 = f2_pack(-mc_new, -mc_new);
-            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};  // 8 partial row sums, as 4 pairs
-            int cnt = 0;
-            uint32_t w[kBlockN / 2], wl[kBlockN / 2];  // wl unused (and eliminated) unless MODE == 2
+                // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
+                uint32_t ov[D];
 #pragma unroll
-            for (int e = 0; e < kBlockN / 2; ++e) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), sl2x2, nmc2), x0, x1);
-                const float p0 = ex2_approx(x0);
-                const float p1 = ex2_approx(x1);
-                ls2[e & 3] = f2_add(ls2[e & 3], f2_pack(p0, p1));
-                w[e] = pack_bf16x2(p0, p1);
-                if (MODE == 2) {
-                    // p - bf16(p) is exact in FP32; hi + lo carries ~16 bits of p
-                    const float h0 = __uint_as_float(w[e] << 16);
-                    const float h1 = __uint_as_float(w[e] & 0xFFFF0000u);
-                    wl[e] = pack_bf16x2(p0 - h0, p1 - h1);
-                }
-                if (STATS) cnt += ((w[e] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((w[e] >> 16) == 0x3F80u ? 1 : 0);
-            }
-            // Pbar_j may overwrite the TMEM Pbar buffer and O may be rescaled
-            // only after O += Pbar_{j-1} V_{j-1} has completed.
-            if (j >= 1) {
-                ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(j - 1) & 1u, p.status);
-                if (!ok) break;
-            }
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                tmem_st16(p_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * h]));
-                if (L::kLoInTmem) tmem_st16(plo_tm + 16 * h, *reinterpret_cast<const uint32_t(*)[16]>(&wl[16 * h]));
-                if (L::kLoInSmem) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int ch = (h & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
-                        st_shared_v4(plo_sm + (h >> 1) * 16384 + sw128_off(row, ch), wl[16 * h + 4 * q],
-                                     wl[16 * h + 4 * q + 1], wl[16 * h + 4 * q + 2], wl[16 * h + 4 * q + 3]);
-                    }
-                }
-            }
-            float lsum;
-            {
-                float a0, a1;
-                f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), a0, a1);
-                lsum = a0 + a1;
-            }
-            l = l * rsc + lsum;
-            if (STATS) {
-                if (changed) ones1 = 0;
-                ones0 += cnt;
-                ones1 += cnt;
-            }
-            // rescale O after the scores are consumed (keeps register use low)
-            if (j >= 1 && __any_sync(0xffffffffu, changed)) {
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(o_tm + c * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
-                    tmem_st32(o_tm + c * 32, r);
-                }
-            }
-            tmem_wait_st();  // Pbar (and any rescaled O) written to TMEM
-            if (L::kLoInSmem) fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(L::kPFull + t));
-        }
-        if (ok && nkt > 0) ok = mbar_wait(bar(L::kODone + t), static_cast<uint32_t>(nkt - 1) & 1u, p.status);
-        const bool store = ok && nkt > 0 && qrow < p.N;
-        const size_t rowid = static_cast<size_t>(bh) * p.N + qrow;
-        if (STATS) {
-            if (store) {
-                p.tie_count[rowid] = C;
-                if (p.p_one) {
-                    p.p_one[rowid] = ones0;
-                    p.p_one[static_cast<size_t>(p.BH) * p.N + rowid] = ones1;
-                }
-            }
-        } else if (nkt > 0 && __all_sync(0xffffffffu, ok)) {
-            // tcgen05.ld is warp-collective: every lane loads, only rows < N store.
-            tc_fence_after();
-            const float inv_l = 1.f / l;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(o_tm + c * 32, r);
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[c * 32]));
                 tmem_wait_ld();
-                if (!store) continue;
-                if (MODE == 2) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + rowid * D + c * 32);
+                tc_fence_before();
+                mbar_arrive(bar(L::kOFree + t));
+                const float inv_l = 1.f / l;
+                if (L::kTmaStoreO) {
+                    // Rows go to the 128-byte-swizzled staging tile (the TMA
+                    // box layout); rows past N are clipped by the TMA store.
+                    const uint32_t stg = MODE == 2 ? plo_sm : sb + L::kOStage + t * L::kOStageBytes;
+                    if (MODE != 2 && ne >= 1) {
+                        ok = stage_free();
+                        if (!ok) break;
+                    }
+                    if (MODE == 2) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv_l, __uint_as_float(r[4 * e + 1]) * inv_l,
-                                             __uint_as_float(r[4 * e + 2]) * inv_l, __uint_as_float(r[4 * e + 3]) * inv_l);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + rowid * D + c * 32);
+                        for (int c = 0; c < D / 4; ++c)  // 16-byte chunks of 4 floats; 32 columns per box
+                            st_shared_v4(stg + (c >> 3) * 16384 + sw128_off(row, c & 7),
+                                         __float_as_uint(__uint_as_float(ov[4 * c]) * inv_l),
+                                         __float_as_uint(__uint_as_float(ov[4 * c + 1]) * inv_l),
+                                         __float_as_uint(__uint_as_float(ov[4 * c + 2]) * inv_l),
+                                         __float_as_uint(__uint_as_float(ov[4 * c + 3]) * inv_l));
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l);
-                        dst[e] = w;
+                        for (int c = 0; c < D / 8; ++c)  // 16-byte chunks of 8 BF16
+                            st_shared_v4(stg + sw128_off(row, c),
+                                         pack_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv_l, __uint_as_float(ov[8 * c + 1]) * inv_l),
+                                         pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv_l, __uint_as_float(ov[8 * c + 3]) * inv_l),
+                                         pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv_l, __uint_as_float(ov[8 * c + 5]) * inv_l),
+                                         pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv_l, __uint_as_float(ov[8 * c + 7]) * inv_l));
+                    }
+                    fence_async_smem();
+                    mbar_arrive(bar(L::kOStaged + t));
+                    if (row == 0) {
+                        ok = mbar_wait(bar(L::kOStaged + t), static_cast<uint32_t>(ne) & 1u, p.status);
+                        if (ok) {
+                            if (MODE == 2) {
+                                tma_store_3d(&tm_o, stg, 0, q0, bh);
+                                tma_store_3d(&tm_o, stg + 16384, 32, q0, bh);
+                            } else {
+                                tma_store_3d(&tm_o, stg, 0, q0, bh);
+                            }
+                            bulk_commit();
+                        }
+                    }
+                } else if (store) {
+                    if (MODE == 2) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + rowid * D);
+#pragma unroll
+                        for (int e = 0; e < D / 4; ++e)
+                            dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
+                                                 __uint_as_float(ov[4 * e + 2]) * inv_l,
+                                                 __uint_as_float(ov[4 * e + 3]) * inv_l);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + rowid * D);
+#pragma unroll
+                        for (int e = 0; e < D / 8; ++e) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
+                            dst[e] = w;
+                        }
                     }
                 }
+                // LSE = m*alpha + ln(l), natural log of the scaled-score normaliser
+                if (store) p.lse[rowid] = (mc + lg2_approx(l)) * 0.69314718055994531f;
             }
-            // LSE = m*alpha + ln(l), natural log of the scaled-score normaliser
-            if (store) p.lse[rowid] = (mc + lg2_approx(l)) * 0.69314718055994531f;
+            ++ne;
         }
     }
 
+    // O's TMA stores complete before the CTA exits
+    if (L::kTmaStoreO && !STATS && warp < kProducerWarp && (threadIdx.x & 127) == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
@@ -490,9 +686,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
-    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>((n_qt + NQ - 1) / NQ));
+    p.n_cq = (n_qt + NQ - 1) / NQ;
+    p.n_items = a.BH * p.n_cq;
+    // persistent: one CTA per SM (or per item, if fewer)
+    const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
     prof_begin(STATS ? 1 : 0, stream);
-    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
     prof_end(STATS ? 1 : 0, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) set_error("fwd launch", e);

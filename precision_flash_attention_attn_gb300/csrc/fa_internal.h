@@ -17,6 +17,7 @@ struct FwdArgs {
     const CUtensorMap* tm_q;
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
+    const CUtensorMap* tm_o;  // O as a TMA store target (the statistics variant ignores it)
     void* o;            // [BH, N, d] BF16 (modes 0, 1) or FP32 (mode 2); null: not written
     float* lse;         // [BH, N]; null: not written
     int32_t* tie_count; // statistics variant only: [BH, N]
@@ -25,6 +26,7 @@ struct FwdArgs {
     float scale;        // alpha
     float scale_log2;   // alpha * log2(e)
     int* status;        // device status word
+    int num_sms;        // persistent grid: at most one CTA per SM
 };
 
 struct BwdArgs {
@@ -45,6 +47,7 @@ struct BwdArgs {
     int BH, N, Npad, d, causal, mode;
     float scale, scale_log2;
     int* status;
+    int num_sms;
 };
 
 struct StatsArgs {

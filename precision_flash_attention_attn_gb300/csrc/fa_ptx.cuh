@@ -267,6 +267,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// One lane of a converged warp (the same lane every time for a full warp).
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// Per-warpgroup register budget changes (all four warps of a warpgroup run
+// the same one; the budgets of all warpgroups must sum to the launch's).
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ math ----
 
 // Packed pairs of FP32 values (one 64-bit register pair) and the paired FP32
