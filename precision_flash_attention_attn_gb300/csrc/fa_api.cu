@@ -211,13 +211,15 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
     float* delta = lse2 + static_cast<size_t>(BH) * Npad;
 
-    CUtensorMap mq, mk, mv, mdo, macc;
+    CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
     rc = FA_OK;
     if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32))
+        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
+        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
         rc = FA_ERR_CUDA;
     if (rc == FA_OK) {
         fa::BwdArgs a{};
@@ -226,6 +228,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         a.tm_v = &mv;
         a.tm_do = &mdo;
         a.tm_dqacc = &macc;
+        a.tm_dk = &mdk;
+        a.tm_dv = &mdv;
         a.o = o;
         a.lse = lse;
         a.dout = dO;
@@ -315,12 +319,14 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
     float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
     float* delta = lse2 + static_cast<size_t>(BH) * Npad;
 
-    CUtensorMap mq, mk, mv, mdo, macc;
+    CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
     if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32))
+        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
+        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
         return FA_ERR_CUDA;
     fa::BwdArgs a{};
     a.tm_q = &mq;
@@ -328,6 +334,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
     a.tm_v = &mv;
     a.tm_do = &mdo;
     a.tm_dqacc = &macc;
+    a.tm_dk = &mdk;
+    a.tm_dv = &mdv;
     a.o = o;
     a.lse = lse;
     a.dout = dO;

@@ -44,76 +44,114 @@ namespace {
 // ------------------------------------------------------------- preprocess --
 
 // D/8 threads per row, 8 elements (16 bytes of dO) each; rows padded to Npad.
+// Each warp works on kUnroll groups of rows at once so that enough loads are
+// in flight to keep HBM busy.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     constexpr int TPR = D / 8;       // threads per row
-    constexpr int RPW = 32 / TPR;    // rows per warp and pass
+    constexpr int RPW = 32 / TPR;    // rows per warp and group
+    constexpr int kUnroll = 4;
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPR;
     const long long rows = static_cast<long long>(a.BH) * a.Npad;
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
     const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
-    for (long long r0 = gw * RPW; r0 < rows; r0 += nwarps * RPW) {
-        const long long r = r0 + lane / TPR;
-        const int bh = static_cast<int>(r / a.Npad);
-        const int i = static_cast<int>(r % a.Npad);
-        const bool valid = r < rows && i < a.N;
-        float acc = 0.f;
-        if (valid) {
-            const size_t base = (static_cast<size_t>(bh) * a.N + i) * D + sub * 8;
-            const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + base);
-            const uint32_t gw4[4] = {g.x, g.y, g.z, g.w};
+    for (long long r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
+        uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
+        bool valid[kUnroll];
+        long long r[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            r[u] = r0 + u * RPW + lane / TPR;
+            const int bh = static_cast<int>(r[u] / a.Npad);
+            const int i = static_cast<int>(r[u] % a.Npad);
+            valid[u] = r[u] < rows && i < a.N;
+            g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (valid[u]) {
+                const size_t base = (static_cast<size_t>(bh) * a.N + i) * D + sub * 8;
+                g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + base);
+                if (a.mode == 2) {
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(a.o) + base);
+                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(a.o) + base + 4);
+                } else {
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + base);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t gw4[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+            float acc = 0.f;
             if (a.mode == 2) {
-                const float4 o0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + base);
-                const float4 o1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + base + 4);
-                const float of[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+                const uint32_t of[8] = {o[u].x, o[u].y, o[u].z, o[u].w, o2[u].x, o2[u].y, o2[u].z, o2[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    acc = fmaf(__uint_as_float(gw4[e] << 16), of[2 * e], acc);
-                    acc = fmaf(__uint_as_float(gw4[e] & 0xFFFF0000u), of[2 * e + 1], acc);
+                    acc = fmaf(__uint_as_float(gw4[e] << 16), __uint_as_float(of[2 * e]), acc);
+                    acc = fmaf(__uint_as_float(gw4[e] & 0xFFFF0000u), __uint_as_float(of[2 * e + 1]), acc);
                 }
             } else {
-                const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + base);
-                const uint32_t ow4[4] = {o.x, o.y, o.z, o.w};
+                const uint32_t ow4[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     acc = fmaf(__uint_as_float(gw4[e] << 16), __uint_as_float(ow4[e] << 16), acc);
                     acc = fmaf(__uint_as_float(gw4[e] & 0xFFFF0000u), __uint_as_float(ow4[e] & 0xFFFF0000u), acc);
                 }
             }
-        }
 #pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (sub == 0 && r < rows) {
-            // stored pre-negated / pre-scaled for the main kernel's FMAs:
-            //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
-            //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
-            a.delta[r] = valid ? -a.scale * acc : 0.f;
-            // padded rows: P = exp2(s - inf) = 0
-            a.lse2[r] = valid ? -a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : -INFINITY;
+            for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (sub == 0 && r[u] < rows) {
+                const int bh = static_cast<int>(r[u] / a.Npad);
+                const int i = static_cast<int>(r[u] % a.Npad);
+                // stored pre-negated / pre-scaled for the main kernel's FMAs:
+                //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
+                //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
+                a.delta[r[u]] = valid[u] ? -a.scale * acc : 0.f;
+                // padded rows: P = exp2(s - inf) = 0
+                a.lse2[r[u]] = valid[u] ? -a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : -INFINITY;
+            }
         }
     }
-    // zero the dQ accumulator
+    // zero the dQ accumulator, four 16-byte stores per thread and pass
     const size_t n4 = static_cast<size_t>(a.BH) * a.N * D / 4;
     float4* acc4 = reinterpret_cast<float4*>(a.dq_acc);
-    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4; e += stride)
-        acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (size_t e = tid; e < n4; e += 4 * nthr) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (e + u * nthr < n4) acc4[e + u * nthr] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
+// dQ workspace (FP32) -> BF16, eight elements per thread and step, four
+// steps' loads in flight.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
                                                          size_t n8) {
-    for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
-         e += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const float4 x = reinterpret_cast<const float4*>(acc)[2 * e];
-        const float4 y = reinterpret_cast<const float4*>(acc)[2 * e + 1];
-        uint4 w;
-        w.x = pack_bf16x2(x.x, x.y);
-        w.y = pack_bf16x2(x.z, x.w);
-        w.z = pack_bf16x2(y.x, y.y);
-        w.w = pack_bf16x2(y.z, y.w);
-        reinterpret_cast<uint4*>(dq)[e] = w;
+    const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (size_t e0 = tid; e0 < n8; e0 += 4 * nthr) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t e = e0 + u * nthr;
+            if (e < n8) {
+                x[u] = reinterpret_cast<const float4*>(acc)[2 * e];
+                y[u] = reinterpret_cast<const float4*>(acc)[2 * e + 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t e = e0 + u * nthr;
+            if (e < n8) {
+                uint4 w;
+                w.x = pack_bf16x2(x[u].x, x[u].y);
+                w.y = pack_bf16x2(x[u].z, x[u].w);
+                w.z = pack_bf16x2(y[u].x, y[u].y);
+                w.w = pack_bf16x2(y[u].z, y[u].w);
+                reinterpret_cast<uint4*>(dq)[e] = w;
+            }
+        }
     }
 }
 
@@ -123,20 +161,30 @@ template <int D>
 struct BwdLayout {
     static constexpr int kTile = kBlockM * D * 2;      // 128 rows x D BF16
     static constexpr int kQStages = (D == 64) ? 2 : 1;
-    static constexpr int kK = 0;
-    static constexpr int kV = kK + kTile;
-    static constexpr int kQ = kV + kTile;                       // [kQStages]
-    static constexpr int kDO = kQ + kQStages * kTile;           // [kQStages]
-    static constexpr int kPt = kDO + kQStages * kTile;          // 128 keys x 128 queries BF16
-    static constexpr int kDSt = kPt + kBlockM * kBlockN * 2;
-    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2; // 8 warps x (32 x 32 FP32), swizzled
-    static constexpr int kLse = kStage + 8 * 4096;              // [kQStages][128] FP32 (-LSE*log2e)
-    static constexpr int kDelta = kLse + kQStages * 512;        // [kQStages][128] FP32 (-alpha*delta)
+    // d = 64: P^T goes to TMEM as the A operand of dV (as Pbar does in the
+    // forward), which frees the shared memory for a second K/V buffer: the
+    // next work item's K and V load while the current one finishes.
+    static constexpr bool kPtInTmem = (D == 64);
+    static constexpr int kKVBufs = (D == 64) ? 2 : 1;
+    static constexpr int kK = 0;                                  // [kKVBufs]
+    static constexpr int kV = kK + kKVBufs * kTile;               // [kKVBufs]
+    static constexpr int kQ = kV + kKVBufs * kTile;               // [kQStages]
+    static constexpr int kDO = kQ + kQStages * kTile;             // [kQStages]
+    static constexpr int kPt = kDO + kQStages * kTile;            // d = 128: 128 keys x 128 queries BF16
+    static constexpr int kDSt = kPt + (kPtInTmem ? 0 : kBlockM * kBlockN * 2);
+    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2;   // 8 warps x (32 x 32 FP32), swizzled
+    static constexpr int kLse = kStage + 8 * 4096;                // [kQStages][128] FP32 (-LSE*log2e)
+    static constexpr int kDelta = kLse + kQStages * 512;          // [kQStages][128] FP32 (-alpha*delta)
     static constexpr int kBar = kDelta + kQStages * 512;
+    // dK/dV epilogue staging (128 key rows, 64-column boxes of 16 KB): the
+    // dS^T buffer holds both at d = 64; at d = 128 dV uses the P^T buffer
+    static constexpr int kEpiDV = kPtInTmem ? kDSt : kPt;
+    static constexpr int kEpiDK = kPtInTmem ? kDSt + kTile : kDSt;
     // barriers
-    static constexpr int kKVFull = 0;
-    static constexpr int kQFull = 1;                       // [kQStages]
-    static constexpr int kQEmpty = kQFull + kQStages;      // [kQStages]
+    static constexpr int kKVFull = 0;                         // [kKVBufs]
+    static constexpr int kKVEmpty = kKVFull + kKVBufs;        // [kKVBufs]
+    static constexpr int kQFull = kKVEmpty + kKVBufs;         // [kQStages]
+    static constexpr int kQEmpty = kQFull + kQStages;         // [kQStages]
     static constexpr int kSFull = kQEmpty + kQStages;
     static constexpr int kSEmpty = kSFull + 1;
     static constexpr int kDPFull = kSEmpty + 1;
@@ -146,8 +194,12 @@ struct BwdLayout {
     static constexpr int kPDSFree = kDSFull + 1;
     static constexpr int kDQFull = kPDSFree + 1;
     static constexpr int kDQEmpty = kDQFull + 1;
-    static constexpr int kDKVDone = kDQEmpty + 1;
-    static constexpr int kNumBars = kDKVDone + 1;
+    static constexpr int kAccDone = kDQEmpty + 1;    // dK, dV of the item complete
+    static constexpr int kAccFree = kAccDone + 1;    // dK, dV read out of TMEM
+    static constexpr int kEpiStaged = kAccFree + 1;  // dK, dV rows in the staging buffers
+    static constexpr int kStageFree = kEpiStaged + 1;  // their TMA stores have read them
+    static constexpr int kDrain = kStageFree + 1;
+    static constexpr int kNumBars = kDrain + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -159,26 +211,39 @@ struct BwdLayout {
     static constexpr uint32_t kColDK = 256 + D;
     static constexpr bool kDQAliasS = (D != 64);  // no room for a separate dQ tile at d = 128
     static constexpr uint32_t kColDQ = kDQAliasS ? kColS : 256 + 2 * D;
+    static constexpr uint32_t kColPt = 256 + 3 * D;  // d = 64: P^T as BF16 pairs, 64 columns
+    static_assert(!kPtInTmem || kColPt + 64 <= 512, "TMEM budget");
     static constexpr uint32_t kMathThreads = 256;  // two warpgroups
 };
 
 struct BwdParams {
     float* lse2;
     float* delta;
-    void* dk;
-    void* dv;
     int BH, N, Npad;
+    int n_kt;     // key tiles per (batch, head)
+    int n_items;  // BH * n_kt
     float scale, scale_log2;
     int* status;
 };
+
+// Work items are (key tile, batch-head) pairs numbered longest first (causal:
+// key tile 0 sees every query tile).  CTA c takes items in a snake order over
+// rounds of gridDim.x, as the forward does.
+__device__ __forceinline__ int bwd_item(int r) {
+    const int G = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    return r * G + ((r & 1) ? G - 1 - c : c);
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dqacc, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
+               const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
     using L = BwdLayout<D>;
     constexpr int QS = L::kQStages;
+    constexpr int KVB = L::kKVBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -187,15 +252,17 @@ __global__ void __launch_bounds__(320, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int kt = blockIdx.y;  // causal: key tile 0 has the most query tiles, runs first
-    const int k0 = kt * kBlockN;
     const int n_qt_all = (p.N + kBlockM - 1) / kBlockM;
-    const int qt_begin = CAUSAL ? kt : 0;
-    const int n_iter = n_qt_all - qt_begin;
+    auto item_bh = [&](int it) { return it % p.BH; };
+    auto item_kt = [&](int it) { return it / p.BH; };
+    auto item_qt0 = [&](int kt) { return CAUSAL ? kt : 0; };          // first query tile
+    auto item_iters = [&](int kt) { return n_qt_all - item_qt0(kt); };  // query tiles visited
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::kKVFull), 1);
+        for (int b = 0; b < KVB; ++b) {
+            mbar_init(bar(L::kKVFull + b), 1);
+            mbar_init(bar(L::kKVEmpty + b), 1);
+        }
         for (int s = 0; s < QS; ++s) {
             mbar_init(bar(L::kQFull + s), 1);
             mbar_init(bar(L::kQEmpty + s), 1);
@@ -209,7 +276,11 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(bar(L::kPDSFree), 1);
         mbar_init(bar(L::kDQFull), 1);
         mbar_init(bar(L::kDQEmpty), L::kMathThreads);
-        mbar_init(bar(L::kDKVDone), 1);
+        mbar_init(bar(L::kAccDone), 1);
+        mbar_init(bar(L::kAccFree), L::kMathThreads);
+        mbar_init(bar(L::kEpiStaged), L::kMathThreads);
+        mbar_init(bar(L::kStageFree), 1);
+        mbar_init(bar(L::kDrain), 1);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -223,131 +294,193 @@ __global__ void __launch_bounds__(320, 1)
 
     if (warp == 8) {
         // -------------------------------------------------------- producer
+        // Per item: K and V (into the item's K/V buffer), then Q, dO and the
+        // per-row LSE/delta of each query tile through the Q ring, running
+        // ahead into the next item as far as the buffers allow.
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
-            mbar_arrive_expect_tx(bar(L::kKVFull), 2 * L::kTile);
-            for (int b = 0; b < D / 64; ++b) {
-                tma_load_3d(sb + L::kK + b * 16384, &tm_k, bar(L::kKVFull), b * 64, k0, bh);
-                tma_load_3d(sb + L::kV + b * 16384, &tm_v, bar(L::kKVFull), b * 64, k0, bh);
-            }
-            int issued = 0;
-            for (int it = 0; it < n_iter; ++it) {
-                const int s = it % QS;
-                const uint32_t u = static_cast<uint32_t>(it / QS);
-                if (it >= QS && !mbar_wait(bar(L::kQEmpty + s), (u - 1) & 1u, p.status)) break;
-                const int q0 = (qt_begin + it) * kBlockM;
-                mbar_arrive_expect_tx(bar(L::kQFull + s), 2 * L::kTile + 1024);
+            bool ok = true;
+            int g = 0;  // query tiles loaded so far (all items)
+            int n = 0;  // items started
+            for (int r = 0; ok; ++r, ++n) {
+                const int itm = bwd_item(r);
+                if (itm >= p.n_items) break;
+                const int bh = item_bh(itm), kt = item_kt(itm);
+                const int kb = n % KVB;
+                if (n >= KVB) ok = mbar_wait(bar(L::kKVEmpty + kb), static_cast<uint32_t>(n / KVB - 1) & 1u, p.status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(L::kKVFull + kb), 2 * L::kTile);
                 for (int b = 0; b < D / 64; ++b) {
-                    tma_load_3d(sb + L::kQ + s * L::kTile + b * 16384, &tm_q, bar(L::kQFull + s), b * 64, q0, bh);
-                    tma_load_3d(sb + L::kDO + s * L::kTile + b * 16384, &tm_do, bar(L::kQFull + s), b * 64, q0, bh);
+                    tma_load_3d(sb + L::kK + kb * L::kTile + b * 16384, &tm_k, bar(L::kKVFull + kb), b * 64,
+                                kt * kBlockN, bh);
+                    tma_load_3d(sb + L::kV + kb * L::kTile + b * 16384, &tm_v, bar(L::kKVFull + kb), b * 64,
+                                kt * kBlockN, bh);
                 }
-                const size_t roff = static_cast<size_t>(bh) * p.Npad + q0;
-                bulk_load(sb + L::kLse + s * 512, p.lse2 + roff, 512, bar(L::kQFull + s));
-                bulk_load(sb + L::kDelta + s * 512, p.delta + roff, 512, bar(L::kQFull + s));
-                issued = it + 1;
+                const int n_iter = item_iters(kt);
+                for (int it = 0; it < n_iter; ++it, ++g) {
+                    const int s = g % QS;
+                    const uint32_t u = static_cast<uint32_t>(g / QS);
+                    if (g >= QS && !(ok = mbar_wait(bar(L::kQEmpty + s), (u - 1) & 1u, p.status))) break;
+                    const int q0 = (item_qt0(kt) + it) * kBlockM;
+                    mbar_arrive_expect_tx(bar(L::kQFull + s), 2 * L::kTile + 1024);
+                    for (int b = 0; b < D / 64; ++b) {
+                        tma_load_3d(sb + L::kQ + s * L::kTile + b * 16384, &tm_q, bar(L::kQFull + s), b * 64, q0, bh);
+                        tma_load_3d(sb + L::kDO + s * L::kTile + b * 16384, &tm_do, bar(L::kQFull + s), b * 64, q0,
+                                    bh);
+                    }
+                    const size_t roff = static_cast<size_t>(bh) * p.Npad + q0;
+                    bulk_load(sb + L::kLse + s * 512, p.lse2 + roff, 512, bar(L::kQFull + s));
+                    bulk_load(sb + L::kDelta + s * 512, p.delta + roff, 512, bar(L::kQFull + s));
+                }
             }
-            mbar_wait(bar(L::kKVFull), 0, p.status);
-            for (int it = issued - QS > 0 ? issued - QS : 0; it < issued; ++it)
-                mbar_wait(bar(L::kQFull + it % QS), static_cast<uint32_t>(it / QS) & 1u, p.status);
+            // Every copy this thread issued must have landed before the CTA
+            // may exit (normally long since true).
+            for (int m = n - KVB > 0 ? n - KVB : 0; m < n; ++m)
+                mbar_wait(bar(L::kKVFull + m % KVB), static_cast<uint32_t>(m / KVB) & 1u, p.status);
+            for (int h = g - QS > 0 ? g - QS : 0; h < g; ++h)
+                mbar_wait(bar(L::kQFull + h % QS), static_cast<uint32_t>(h / QS) & 1u, p.status);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdSS = idesc_bf16(kBlockM, kBlockN, false, false);  // S^T, dP^T
-            constexpr uint32_t kIdAcc = idesc_bf16(kBlockM, D, false, true);         // dV, dK
-            constexpr uint32_t kIdDQ = idesc_bf16(kBlockM, D, true, true);           // dQ
-            bool ok = mbar_wait(bar(L::kKVFull), 0, p.status);
-            // S^T(it) = K Q^T
-            auto issue_s = [&](int it) {
-                const int s = it % QS;
-                ok = ok && mbar_wait(bar(L::kQFull + s), static_cast<uint32_t>(it / QS) & 1u, p.status);
-                if (ok && it >= 1) ok = mbar_wait(bar(L::kSEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
-                if (ok && it >= 1 && L::kDQAliasS)
-                    ok = mbar_wait(bar(L::kDQEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+        // The whole warp runs the loop and waits; one elected lane issues each
+        // group of MMAs together with the commits that track them.
+        constexpr uint32_t kIdSS = idesc_bf16(kBlockM, kBlockN, false, false);  // S^T, dP^T
+        constexpr uint32_t kIdAcc = idesc_bf16(kBlockM, D, false, true);         // dV, dK
+        constexpr uint32_t kIdDQ = idesc_bf16(kBlockM, D, true, true);           // dQ
+        auto wait_all = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
+        };
+        bool ok = true;
+        bool issued = false;
+        int g = 0;  // query tiles processed so far (all items)
+        for (int r = 0, n = 0; ok; ++r, ++n) {
+            const int itm = bwd_item(r);
+            if (itm >= p.n_items) break;
+            const int kt = item_kt(itm);
+            const int n_iter = item_iters(kt);
+            const int kb = n % KVB;
+            const uint32_t sK = sb + L::kK + kb * L::kTile;
+            const uint32_t sV = sb + L::kV + kb * L::kTile;
+            ok = wait_all(bar(L::kKVFull + kb), static_cast<uint32_t>(n / KVB) & 1u);
+            if (!ok) break;
+            // S^T(gi) = K Q^T
+            auto issue_s = [&](int gi) {
+                const int s = gi % QS;
+                ok = ok && wait_all(bar(L::kQFull + s), static_cast<uint32_t>(gi / QS) & 1u);
+                if (ok && gi >= 1) ok = wait_all(bar(L::kSEmpty), static_cast<uint32_t>(gi - 1) & 1u);
+                if (ok && gi >= 1 && L::kDQAliasS) ok = wait_all(bar(L::kDQEmpty), static_cast<uint32_t>(gi - 1) & 1u);
                 if (!ok) return;
                 tc_fence_after();
                 const uint32_t sQ = sb + L::kQ + s * L::kTile;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + L::kColS, sdesc_sw128(sb + L::kK + ko, 16, 1024), sdesc_sw128(sQ + ko, 16, 1024),
-                                kIdSS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16_ss(tmem + L::kColS, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ + ko, 16, 1024),
+                                    kIdSS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(L::kSFull));
                 }
-                mma_commit(bar(L::kSFull));
+                __syncwarp();
+                issued = true;
             };
-            // dP^T(it) = V dO^T   (Q/dO stage it is already known to be loaded)
-            auto issue_dp = [&](int it) {
-                const int s = it % QS;
-                if (ok && it >= 1) ok = mbar_wait(bar(L::kDPEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+            // dP^T(gi) = V dO^T   (Q/dO stage gi is already known to be loaded)
+            auto issue_dp = [&](int gi) {
+                const int s = gi % QS;
+                if (ok && gi >= 1) ok = wait_all(bar(L::kDPEmpty), static_cast<uint32_t>(gi - 1) & 1u);
                 if (!ok) return;
                 tc_fence_after();
                 const uint32_t sDO = sb + L::kDO + s * L::kTile;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(sb + L::kV + ko, 16, 1024), sdesc_sw128(sDO + ko, 16, 1024),
-                                kIdSS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sDO + ko, 16, 1024),
+                                    kIdSS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(L::kDPFull));
                 }
-                mma_commit(bar(L::kDPFull));
+                __syncwarp();
             };
             // Software pipeline: the next tile's S^T (and dP^T) are issued
             // ahead of this tile's dK/dQ products, so the P^T/dS^T warps find
             // their next scores ready.  With dQ aliasing S^T (d = 128) the next
             // S^T must instead wait for this tile's dQ to be drained.
-            if (n_iter > 0) {
-                issue_s(0);
-                issue_dp(0);
-            }
-            for (int it = 0; it < n_iter && ok; ++it) {
-                const int s = it % QS;
-                const uint32_t cur = static_cast<uint32_t>(it) & 1u;
+            issue_s(g);
+            issue_dp(g);
+            for (int it = 0; it < n_iter && ok; ++it, ++g) {
+                const int s = g % QS;
+                const uint32_t cur = static_cast<uint32_t>(g) & 1u;
                 const uint32_t sQ = sb + L::kQ + s * L::kTile;
                 const uint32_t sDO = sb + L::kDO + s * L::kTile;
-                // dV += P^T dO
-                ok = mbar_wait(bar(L::kPFull), cur, p.status);
+                // dV += P^T dO; the item's first product overwrites dV, which
+                // the previous item's epilogue must have read out
+                ok = wait_all(bar(L::kPFull), cur);
+                if (ok && it == 0 && n >= 1) ok = wait_all(bar(L::kAccFree), static_cast<uint32_t>(n - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBlockM / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(sb + L::kPt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sDO + kk * 2048, 16384, 1024);
-                    mma_bf16_ss(tmem + L::kColDV, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                        const uint64_t b = sdesc_sw128(sDO + kk * 2048, 16384, 1024);
+                        if (L::kPtInTmem) {
+                            mma_bf16_ts(tmem + L::kColDV, tmem + L::kColPt + kk * 8, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t a = sdesc_sw128(sb + L::kPt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            mma_bf16_ss(tmem + L::kColDV, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
                 }
-                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(it + 1);
+                __syncwarp();
+                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(g + 1);
                 if (!ok) break;
                 // dK += dS^T Q
-                ok = mbar_wait(bar(L::kDSFull), cur, p.status);
+                ok = wait_all(bar(L::kDSFull), cur);
                 if (!ok) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBlockM / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(sb + L::kDSt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(sQ + kk * 2048, 16384, 1024);
-                    mma_bf16_ss(tmem + L::kColDK, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(sb + L::kDSt + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = sdesc_sw128(sQ + kk * 2048, 16384, 1024);
+                        mma_bf16_ss(tmem + L::kColDK, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
+                __syncwarp();
                 // dQ_t = dS K  (A = dS^T buffer read M-major, B = K read N-major)
-                if (!L::kDQAliasS && it >= 1) ok = mbar_wait(bar(L::kDQEmpty), static_cast<uint32_t>(it - 1) & 1u, p.status);
+                if (!L::kDQAliasS && g >= 1) ok = wait_all(bar(L::kDQEmpty), static_cast<uint32_t>(g - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(sb + L::kDSt + kk * 2048, 16384, 1024);
-                    const uint64_t b = sdesc_sw128(sb + L::kK + kk * 2048, 16384, 1024);
-                    mma_bf16_ss(tmem + L::kColDQ, a, b, kIdDQ, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                        const uint64_t a = sdesc_sw128(sb + L::kDSt + kk * 2048, 16384, 1024);
+                        const uint64_t b = sdesc_sw128(sK + kk * 2048, 16384, 1024);
+                        mma_bf16_ss(tmem + L::kColDQ, a, b, kIdDQ, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(L::kDQFull));
+                    mma_commit(bar(L::kQEmpty + s));
+                    mma_commit(bar(L::kPDSFree));
+                    if (it + 1 == n_iter) {
+                        mma_commit(bar(L::kKVEmpty + kb));  // last read of this item's K and V
+                        mma_commit(bar(L::kAccDone));
+                    }
                 }
-                mma_commit(bar(L::kDQFull));
-                mma_commit(bar(L::kQEmpty + s));
-                mma_commit(bar(L::kPDSFree));
+                __syncwarp();
                 if (it + 1 < n_iter) {
-                    if (L::kDQAliasS) issue_s(it + 1);
-                    issue_dp(it + 1);
+                    if (L::kDQAliasS) issue_s(g + 1);
+                    issue_dp(g + 1);
                 }
             }
-            mma_commit(bar(L::kDKVDone));
-            mbar_wait(bar(L::kDKVDone), 0, p.status);
+        }
+        // Drain: every MMA this warp issued has completed before TMEM is freed.
+        if (issued) {
+            if (elect_one()) mma_commit(bar(L::kDrain));
+            __syncwarp();
+            mbar_wait(bar(L::kDrain), 0, p.status);
         }
     } else {
         // ------------------------- math warpgroups: P^T, dS^T, dQ drain, dK/dV
@@ -359,16 +492,19 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
         const uint64_t alx2 = f2_pack(p.scale, p.scale);
         const uint32_t stage = sb + L::kStage + (warp & 7) * 4096;
+        auto wait_w = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
+        };
         bool ok = true;
+        int g = 0;  // query tiles processed so far (all items)
 
-        // Drain dQ of query tile `jt`: this warp's 32 query rows, this
-        // warpgroup's half of the d columns, as 32 x 32 FP32 boxes added into
-        // the workspace with TMA reduce-add.
-        auto drain_dq = [&](int jt) -> bool {
-            bool good = mbar_wait(bar(L::kDQFull), static_cast<uint32_t>(jt) & 1u, p.status);
-            if (!__all_sync(0xffffffffu, good)) return false;
+        // Drain dQ of query tile `qt` (global tile count gi): this warp's 32
+        // query rows, this warpgroup's half of the d columns, as 32 x 32 FP32
+        // boxes added into the workspace with TMA reduce-add.
+        auto drain_dq = [&](int gi, int qt, int bh) -> bool {
+            if (!wait_w(bar(L::kDQFull), static_cast<uint32_t>(gi) & 1u)) return false;
             tc_fence_after();
-            const int q0 = (qt_begin + jt) * kBlockM;
+            const int q0 = qt * kBlockM;
 #pragma unroll
             for (int cb = 0; cb < D / 64; ++cb) {
                 const int col = wg * (D / 2) + cb * 32;
@@ -394,143 +530,189 @@ __global__ void __launch_bounds__(320, 1)
             return true;
         };
 
-        for (int it = 0; it < n_iter; ++it) {
-            const int s = it % QS;
-            const uint32_t u = static_cast<uint32_t>(it / QS);
-            const uint32_t cur = static_cast<uint32_t>(it) & 1u;
-            const int qt = qt_begin + it;
-            if (L::kDQAliasS && it >= 1) {
-                // dQ shares the S^T columns: drain it before the next S^T lands
-                ok = drain_dq(it - 1);
-                if (!ok) break;
-            }
-            ok = mbar_wait(bar(L::kSFull), cur, p.status) && mbar_wait(bar(L::kQFull + s), u & 1u, p.status);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float4* nl4 = reinterpret_cast<const float4*>(smem + L::kLse + s * 512) + c0 / 4;
-            const float4* nd4 = reinterpret_cast<const float4*>(smem + L::kDelta + s * 512) + c0 / 4;
-            float pr[64];
-            {
-                uint32_t r[2][32];
-                tmem_ld32(tmem + lane_off + L::kColS + c0, r[0]);
-                tmem_ld32(tmem + lane_off + L::kColS + c0 + 32, r[1]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar(L::kSEmpty));
-                // P^T[kr][q] = exp2(s * alpha*log2e - LSE_q*log2e)
-#pragma unroll
-                for (int g = 0; g < 16; ++g) {
-                    const float4 n = nl4[g];
-                    const uint32_t* rr = &r[g >> 3][(g & 7) * 4];
-                    float x0, x1, x2, x3;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[0]), __uint_as_float(rr[1])), sl2x2, f2_pack(n.x, n.y)),
-                              x0, x1);
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2]), __uint_as_float(rr[3])), sl2x2, f2_pack(n.z, n.w)),
-                              x2, x3);
-                    pr[4 * g] = ex2_approx(x0);
-                    pr[4 * g + 1] = ex2_approx(x1);
-                    pr[4 * g + 2] = ex2_approx(x2);
-                    pr[4 * g + 3] = ex2_approx(x3);
+        for (int r = 0, n = 0; ok; ++r, ++n) {
+            const int itm = bwd_item(r);
+            if (itm >= p.n_items) break;
+            const int bh = item_bh(itm), kt = item_kt(itm);
+            const int qt_begin = item_qt0(kt);
+            const int n_iter = item_iters(kt);
+            for (int it = 0; it < n_iter; ++it, ++g) {
+                const int s = g % QS;
+                const uint32_t u = static_cast<uint32_t>(g / QS);
+                const uint32_t cur = static_cast<uint32_t>(g) & 1u;
+                const int qt = qt_begin + it;
+                if (L::kDQAliasS && it >= 1) {
+                    // dQ shares the S^T columns: drain it before the next S^T lands
+                    ok = drain_dq(g - 1, qt - 1, bh);
+                    if (!ok) break;
                 }
-            }
-            if (CAUSAL && qt == kt) {
-                // diagonal tile: query q sees key kr only if q >= kr
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c0 + c < kr) pr[c] = 0.f;
-            }
-            if (it >= 1) {
-                ok = mbar_wait(bar(L::kPDSFree), static_cast<uint32_t>(it - 1) & 1u, p.status);
+                ok = wait_w(bar(L::kSFull), cur) && wait_w(bar(L::kQFull + s), u & 1u);
                 if (!ok) break;
-            }
-            const uint32_t pt_blk = sb + L::kPt + wg * 16384;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int c = ch * 8;
-                st_shared_v4(pt_blk + sw128_off(kr, ch), pack_bf16x2(pr[c], pr[c + 1]), pack_bf16x2(pr[c + 2], pr[c + 3]),
-                             pack_bf16x2(pr[c + 4], pr[c + 5]), pack_bf16x2(pr[c + 6], pr[c + 7]));
-            }
-            fence_async_smem();
-            mbar_arrive(bar(L::kPFull));
-            if (!L::kDQAliasS && it >= 1) {
-                // the previous tile's dQ has been computed meanwhile
-                ok = drain_dq(it - 1);
-                if (!ok) break;
-            }
-            // dS^T[kr][q] = P * (alpha * dP + (-alpha * delta_q))
-            ok = mbar_wait(bar(L::kDPFull), cur, p.status);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t ds_blk = sb + L::kDSt + wg * 16384;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kColDP + c0 + h * 32, r);
-                tmem_wait_ld();
-                if (h == 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(L::kDPEmpty));
-                }
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {  // 8 queries per group
-                    const int c = h * 32 + g * 8;
-                    const float4 na = nd4[c / 4];
-                    const float4 nb = nd4[c / 4 + 1];
-                    const uint32_t* rr = &r[g * 8];
-                    float d[8];
-                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[0]), __uint_as_float(rr[1])), alx2, f2_pack(na.x, na.y)),
-                                     f2_pack(pr[c], pr[c + 1])), d[0], d[1]);
-                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[2]), __uint_as_float(rr[3])), alx2, f2_pack(na.z, na.w)),
-                                     f2_pack(pr[c + 2], pr[c + 3])), d[2], d[3]);
-                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[4]), __uint_as_float(rr[5])), alx2, f2_pack(nb.x, nb.y)),
-                                     f2_pack(pr[c + 4], pr[c + 5])), d[4], d[5]);
-                    f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rr[6]), __uint_as_float(rr[7])), alx2, f2_pack(nb.z, nb.w)),
-                                     f2_pack(pr[c + 6], pr[c + 7])), d[6], d[7]);
-                    st_shared_v4(ds_blk + sw128_off(kr, c >> 3), pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]),
-                                 pack_bf16x2(d[4], d[5]), pack_bf16x2(d[6], d[7]));
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(bar(L::kDSFull));
-        }
-        if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
-        if (lane == 0) bulk_wait0();
-        // dK, dV epilogue: key rows, this warpgroup's half of the d columns
-        if (ok) ok = mbar_wait(bar(L::kDKVDone), 0, p.status);
-        if (__all_sync(0xffffffffu, ok)) {
-            tc_fence_after();
-            const int krow = k0 + kr;
-            const bool store = krow < p.N;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk);
-                const uint32_t col = (which == 0 ? L::kColDV : L::kColDK) + wg * (D / 2);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_off + col + c * 32, r);
+                tc_fence_after();
+                const float4* nl4 = reinterpret_cast<const float4*>(smem + L::kLse + s * 512) + c0 / 4;
+                const float4* nd4 = reinterpret_cast<const float4*>(smem + L::kDelta + s * 512) + c0 / 4;
+                float pr[64];
+                {
+                    uint32_t rr2[2][32];
+                    tmem_ld32(tmem + lane_off + L::kColS + c0, rr2[0]);
+                    tmem_ld32(tmem + lane_off + L::kColS + c0 + 32, rr2[1]);
                     tmem_wait_ld();
-                    if (!store) continue;
-                    uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * p.N + krow) * D + wg * (D / 2) +
-                                                          c * 32);
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kSEmpty));
+                    // P^T[kr][q] = exp2(s * alpha*log2e - LSE_q*log2e)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]), __uint_as_float(r[8 * e + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]), __uint_as_float(r[8 * e + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]), __uint_as_float(r[8 * e + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]), __uint_as_float(r[8 * e + 7]));
-                        dst[e] = w;
+                    for (int gg = 0; gg < 16; ++gg) {
+                        const float4 nv = nl4[gg];
+                        const uint32_t* rr = &rr2[gg >> 3][(gg & 7) * 4];
+                        float x0, x1, x2, x3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[0]), __uint_as_float(rr[1])), sl2x2,
+                                         f2_pack(nv.x, nv.y)),
+                                  x0, x1);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[2]), __uint_as_float(rr[3])), sl2x2,
+                                         f2_pack(nv.z, nv.w)),
+                                  x2, x3);
+                        pr[4 * gg] = ex2_approx(x0);
+                        pr[4 * gg + 1] = ex2_approx(x1);
+                        pr[4 * gg + 2] = ex2_approx(x2);
+                        pr[4 * gg + 3] = ex2_approx(x3);
                     }
                 }
+                if (CAUSAL && qt == kt) {
+                    // diagonal tile: query q sees key kr only if q >= kr
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c0 + c < kr) pr[c] = 0.f;
+                }
+                if (g >= 1) {
+                    ok = wait_w(bar(L::kPDSFree), static_cast<uint32_t>(g - 1) & 1u);
+                    if (!ok) break;
+                }
+                if (it == 0 && n >= 1) {
+                    // the previous item's dK/dV stores have read the staging buffers
+                    if (threadIdx.x == 0) {
+                        bulk_wait_read0();
+                        mbar_arrive(bar(L::kStageFree));
+                    }
+                    ok = wait_w(bar(L::kStageFree), static_cast<uint32_t>(n - 1) & 1u);
+                    if (!ok) break;
+                }
+                if (L::kPtInTmem) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+                    tmem_st32(tmem + lane_off + L::kColPt + wg * 32, w);
+                    tmem_wait_st();
+                    tc_fence_before();
+                } else {
+                    const uint32_t pt_blk = sb + L::kPt + wg * 16384;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const int c = ch * 8;
+                        st_shared_v4(pt_blk + sw128_off(kr, ch), pack_bf16x2(pr[c], pr[c + 1]),
+                                     pack_bf16x2(pr[c + 2], pr[c + 3]), pack_bf16x2(pr[c + 4], pr[c + 5]),
+                                     pack_bf16x2(pr[c + 6], pr[c + 7]));
+                    }
+                    fence_async_smem();
+                }
+                mbar_arrive(bar(L::kPFull));
+                if (!L::kDQAliasS && it >= 1) {
+                    // the previous tile's dQ has been computed meanwhile
+                    ok = drain_dq(g - 1, qt - 1, bh);
+                    if (!ok) break;
+                }
+                // dS^T[kr][q] = P * (alpha * dP + (-alpha * delta_q))
+                ok = wait_w(bar(L::kDPFull), cur);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ds_blk = sb + L::kDSt + wg * 16384;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + lane_off + L::kColDP + c0 + h * 32, rr);
+                    tmem_wait_ld();
+                    if (h == 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(L::kDPEmpty));
+                    }
+#pragma unroll
+                    for (int gq = 0; gq < 4; ++gq) {  // 8 queries per group
+                        const int c = h * 32 + gq * 8;
+                        const float4 na = nd4[c / 4];
+                        const float4 nb = nd4[c / 4 + 1];
+                        const uint32_t* rv = &rr[gq * 8];
+                        float dv8[8];
+                        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[0]), __uint_as_float(rv[1])), alx2,
+                                                f2_pack(na.x, na.y)),
+                                         f2_pack(pr[c], pr[c + 1])),
+                                  dv8[0], dv8[1]);
+                        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[2]), __uint_as_float(rv[3])), alx2,
+                                                f2_pack(na.z, na.w)),
+                                         f2_pack(pr[c + 2], pr[c + 3])),
+                                  dv8[2], dv8[3]);
+                        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[4]), __uint_as_float(rv[5])), alx2,
+                                                f2_pack(nb.x, nb.y)),
+                                         f2_pack(pr[c + 4], pr[c + 5])),
+                                  dv8[4], dv8[5]);
+                        f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[6]), __uint_as_float(rv[7])), alx2,
+                                                f2_pack(nb.z, nb.w)),
+                                         f2_pack(pr[c + 6], pr[c + 7])),
+                                  dv8[6], dv8[7]);
+                        st_shared_v4(ds_blk + sw128_off(kr, c >> 3), pack_bf16x2(dv8[0], dv8[1]),
+                                     pack_bf16x2(dv8[2], dv8[3]), pack_bf16x2(dv8[4], dv8[5]),
+                                     pack_bf16x2(dv8[6], dv8[7]));
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(bar(L::kDSFull));
+            }
+            if (!ok) break;
+            ok = drain_dq(g - 1, qt_begin + n_iter - 1, bh);
+            if (!ok) break;
+            // ------------------------------------------------ dK/dV epilogue
+            // Key rows, this warpgroup's half of the d columns: read out of
+            // TMEM (which frees the accumulators for the next item), staged as
+            // BF16 in 128-byte-swizzled 64-column boxes, written by TMA (rows
+            // past N are clipped).
+            ok = wait_w(bar(L::kAccDone), static_cast<uint32_t>(n) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t acc[2][D / 2];
+#pragma unroll
+            for (int which = 0; which < 2; ++which)
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tmem_ld32(tmem + lane_off + (which == 0 ? L::kColDV : L::kColDK) + wg * (D / 2) + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&acc[which][c * 32]));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(L::kAccFree));
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t base = sb + (which == 0 ? L::kEpiDV : L::kEpiDK);
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 8) {
+                    const int col = wg * (D / 2) + c;  // column within the d columns
+                    st_shared_v4(base + (col >> 6) * 16384 + sw128_off(kr, (col & 63) >> 3),
+                                 pack_bf16x2(__uint_as_float(acc[which][c]), __uint_as_float(acc[which][c + 1])),
+                                 pack_bf16x2(__uint_as_float(acc[which][c + 2]), __uint_as_float(acc[which][c + 3])),
+                                 pack_bf16x2(__uint_as_float(acc[which][c + 4]), __uint_as_float(acc[which][c + 5])),
+                                 pack_bf16x2(__uint_as_float(acc[which][c + 6]), __uint_as_float(acc[which][c + 7])));
+                }
+            }
+            fence_async_smem();
+            mbar_arrive(bar(L::kEpiStaged));
+            if (threadIdx.x == 0) {
+                ok = mbar_wait(bar(L::kEpiStaged), static_cast<uint32_t>(n) & 1u, p.status);
+                if (ok) {
+                    for (int b = 0; b < D / 64; ++b) {
+                        tma_store_3d(&tm_dv, sb + L::kEpiDV + b * 16384, b * 64, kt * kBlockN, bh);
+                        tma_store_3d(&tm_dk, sb + L::kEpiDK + b * 16384, b * 64, kt * kBlockN, bh);
+                    }
+                    bulk_commit();
+                }
             }
         }
+        if (lane == 0) bulk_wait0();
     }
 
     tc_fence_before();
@@ -553,18 +735,19 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     BwdParams p;
     p.lse2 = a.lse2;
     p.delta = a.delta;
-    p.dk = a.dk;
-    p.dv = a.dv;
     p.BH = a.BH;
     p.N = a.N;
     p.Npad = a.Npad;
+    p.n_kt = (a.N + kBlockN - 1) / kBlockN;
+    p.n_items = a.BH * p.n_kt;
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
-    const int n_kt = (a.N + kBlockN - 1) / kBlockN;
-    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(n_kt));
+    // persistent: one CTA per SM (or per item, if fewer)
+    const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
     prof_begin(3, stream);
-    kern<<<grid, 320, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, p);
+    kern<<<grid, 320, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
     prof_end(3, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -594,9 +777,9 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
     const int sms = num_sms();
     prof_begin(2, stream);
     if (a.d == 64)
-        bwd_pre_kernel<64><<<sms * 4, 256, 0, stream>>>(a);
+        bwd_pre_kernel<64><<<sms * 8, 256, 0, stream>>>(a);
     else
-        bwd_pre_kernel<128><<<sms * 4, 256, 0, stream>>>(a);
+        bwd_pre_kernel<128><<<sms * 8, 256, 0, stream>>>(a);
     prof_end(2, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -610,7 +793,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const size_t n8 = static_cast<size_t>(a.BH) * a.N * a.d / 8;
     prof_begin(4, stream);
-    dq_convert_kernel<<<sms * 4, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8);
+    dq_convert_kernel<<<sms * 8, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8);
     prof_end(4, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) set_error("dq_convert launch", e);
