@@ -53,19 +53,22 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     constexpr int kUnroll = 4;
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPR;
-    const long long rows = static_cast<long long>(a.BH) * a.Npad;
-    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // rows < 2^31 (BH * Npad * d is checked against it), so 32-bit index math
+    const int rows = a.BH * a.Npad;
+    const int nwarps = static_cast<int>(gridDim.x) * (blockDim.x >> 5);
+    const int gw = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
-    for (long long r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
+    for (int r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
         uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
         bool valid[kUnroll];
-        long long r[kUnroll];
+        int r[kUnroll], bhs[kUnroll], is[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             r[u] = r0 + u * RPW + lane / TPR;
-            const int bh = static_cast<int>(r[u] / a.Npad);
-            const int i = static_cast<int>(r[u] % a.Npad);
+            const int bh = r[u] / a.Npad;
+            const int i = r[u] - bh * a.Npad;
+            bhs[u] = bh;
+            is[u] = i;
             valid[u] = r[u] < rows && i < a.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
             if (valid[u]) {
@@ -101,8 +104,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 #pragma unroll
             for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (sub == 0 && r[u] < rows) {
-                const int bh = static_cast<int>(r[u] / a.Npad);
-                const int i = static_cast<int>(r[u] % a.Npad);
+                const int bh = bhs[u];
+                const int i = is[u];
                 // stored pre-negated / pre-scaled for the main kernel's FMAs:
                 //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
                 //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
