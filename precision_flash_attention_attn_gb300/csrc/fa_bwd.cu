@@ -25,9 +25,10 @@
 //                    Warp roles: two math warpgroups (warps 0-3: query
 //                    columns 0-63 of the tile, warps 4-7: columns 64-127;
 //                    thread t of a warpgroup owns key row t) recompute P^T and
-//                    dS^T, drain each dQ tile from TMEM into the reduce-add
-//                    (one 32-row box per warp), and finally store dK and dV;
-//                    warp 8 issues TMA loads; warp 9 issues the MMAs.  The
+//                    dS^T and finally store dK and dV; a drain warpgroup
+//                    (warps 8-11, one TMEM lane quarter each) moves each dQ
+//                    tile from TMEM into the reduce-add, off the math chain;
+//                    warp 12 issues TMA loads; warp 13 issues the MMAs.  The
 //                    next tile's S^T and dP^T are issued ahead of the current
 //                    tile's dK/dQ products.
 //   dq_convert_kernel  dQ workspace (FP32) -> BF16.
@@ -163,7 +164,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 template <int D>
 struct BwdLayout {
     static constexpr int kTile = kBlockM * D * 2;      // 128 rows x D BF16
-    static constexpr int kQStages = (D == 64) ? 2 : 1;
+    // d = 64: three Q/dO stages, so the next query tile's S^T can be issued
+    // while the current one is still being worked on
+    static constexpr int kQStages = (D == 64) ? 3 : 1;
     // d = 64: P^T goes to TMEM as the A operand of dV (as Pbar does in the
     // forward), which frees the shared memory for a second K/V buffer: the
     // next work item's K and V load while the current one finishes.
@@ -175,8 +178,8 @@ struct BwdLayout {
     static constexpr int kDO = kQ + kQStages * kTile;             // [kQStages]
     static constexpr int kPt = kDO + kQStages * kTile;            // d = 128: 128 keys x 128 queries BF16
     static constexpr int kDSt = kPt + (kPtInTmem ? 0 : kBlockM * kBlockN * 2);
-    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2;   // 8 warps x (32 x 32 FP32), swizzled
-    static constexpr int kLse = kStage + 8 * 4096;                // [kQStages][128] FP32 (-LSE*log2e)
+    static constexpr int kStage = kDSt + kBlockM * kBlockN * 2;   // 4 drain warps x (32 x 32 FP32), swizzled
+    static constexpr int kLse = kStage + 4 * 4096;                // [kQStages][128] FP32 (-LSE*log2e)
     static constexpr int kDelta = kLse + kQStages * 512;          // [kQStages][128] FP32 (-alpha*delta)
     static constexpr int kBar = kDelta + kQStages * 512;
     // dK/dV epilogue staging (128 key rows, 64-column boxes of 16 KB): the
@@ -217,6 +220,15 @@ struct BwdLayout {
     static constexpr uint32_t kColPt = 256 + 3 * D;  // d = 64: P^T as BF16 pairs, 64 columns
     static_assert(!kPtInTmem || kColPt + 64 <= 512, "TMEM budget");
     static constexpr uint32_t kMathThreads = 256;  // two warpgroups
+    static constexpr uint32_t kDrainThreads = 128; // one warpgroup
+    static constexpr int kDrainWarp0 = 8;
+    static constexpr int kProducerWarp = 12;
+    static constexpr int kMmaWarp = 13;            // warps 14, 15 idle (whole warpgroups for setmaxnreg)
+    static constexpr int kThreads = 512;
+    // registers: 2 x 128 x 168 (math) + 2 x 128 x 88 (drain, producer, MMA) = 512 x 128
+    static constexpr uint32_t kRegsMath = 168;
+    static constexpr uint32_t kRegsOther = 88;
+    static_assert(256 * kRegsMath + 256 * kRegsOther == kThreads * 128, "register split");
 };
 
 struct BwdParams {
@@ -239,7 +251,7 @@ __device__ __forceinline__ int bwd_item(int r) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(bar(L::kDSFull), L::kMathThreads);
         mbar_init(bar(L::kPDSFree), 1);
         mbar_init(bar(L::kDQFull), 1);
-        mbar_init(bar(L::kDQEmpty), L::kMathThreads);
+        mbar_init(bar(L::kDQEmpty), L::kDrainThreads);
         mbar_init(bar(L::kAccDone), 1);
         mbar_init(bar(L::kAccFree), L::kMathThreads);
         mbar_init(bar(L::kEpiStaged), L::kMathThreads);
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(bar(L::kDrain), 1);
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == L::kMmaWarp) {
         tmem_alloc(sb + L::kTmemSlot, 512);
         tmem_relinquish();
     }
@@ -295,7 +307,9 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-    if (warp == 8) {
+    if (warp >= L::kDrainWarp0) {
+    regs_dec<L::kRegsOther>();
+    if (warp == L::kProducerWarp) {
         // -------------------------------------------------------- producer
         // Per item: K and V (into the item's K/V buffer), then Q, dO and the
         // per-row LSE/delta of each query tile through the Q ring, running
@@ -346,7 +360,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int h = g - QS > 0 ? g - QS : 0; h < g; ++h)
                 mbar_wait(bar(L::kQFull + h % QS), static_cast<uint32_t>(h / QS) & 1u, p.status);
         }
-    } else if (warp == 9) {
+    } else if (warp == L::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
         // The whole warp runs the loop and waits; one elected lane issues each
         // group of MMAs together with the commits that track them.
@@ -408,10 +422,11 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 __syncwarp();
             };
-            // Software pipeline: the next tile's S^T (and dP^T) are issued
-            // ahead of this tile's dK/dQ products, so the P^T/dS^T warps find
-            // their next scores ready.  With dQ aliasing S^T (d = 128) the next
-            // S^T must instead wait for this tile's dQ to be drained.
+            // Software pipeline: the next tile's S^T is issued as soon as the math
+            // warps have read this tile's S^T, and the next dP^T as soon as they
+            // have read this dP^T, so both are ready before the math warps ask.
+            // With dQ aliasing S^T (d = 128) the next S^T must instead wait for
+            // this tile's dQ to be drained, after the dQ product.
             issue_s(g);
             issue_dp(g);
             for (int it = 0; it < n_iter && ok; ++it, ++g) {
@@ -419,9 +434,10 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t cur = static_cast<uint32_t>(g) & 1u;
                 const uint32_t sQ = sb + L::kQ + s * L::kTile;
                 const uint32_t sDO = sb + L::kDO + s * L::kTile;
+                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(g + 1);
                 // dV += P^T dO; the item's first product overwrites dV, which
                 // the previous item's epilogue must have read out
-                ok = wait_all(bar(L::kPFull), cur);
+                ok = ok && wait_all(bar(L::kPFull), cur);
                 if (ok && it == 0 && n >= 1) ok = wait_all(bar(L::kAccFree), static_cast<uint32_t>(n - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(320, 1)
                     }
                 }
                 __syncwarp();
-                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(g + 1);
+                if (!L::kDQAliasS && it + 1 < n_iter) issue_dp(g + 1);
                 if (!ok) break;
                 // dK += dS^T Q
                 ok = wait_all(bar(L::kDSFull), cur);
@@ -473,8 +489,8 @@ __global__ void __launch_bounds__(320, 1)
                     }
                 }
                 __syncwarp();
-                if (it + 1 < n_iter) {
-                    if (L::kDQAliasS) issue_s(g + 1);
+                if (L::kDQAliasS && it + 1 < n_iter) {
+                    issue_s(g + 1);
                     issue_dp(g + 1);
                 }
             }
@@ -485,8 +501,65 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             mbar_wait(bar(L::kDrain), 0, p.status);
         }
+    } else if (warp < L::kDrainWarp0 + 4) {
+        // ------------------------------------------------- dQ drain warpgroup
+        // Per query tile: this warp's 32 query rows (its TMEM lane quarter) of
+        // dQ, read out of TMEM 64 columns at a time, staged as 32 x 32 FP32
+        // boxes (one buffer per warp) and added into the workspace with TMA
+        // reduce-add.  The tile's TMEM columns are released as soon as the last
+        // columns are in registers.
+        const int wq = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t stg = sb + L::kStage + wq * 4096;
+        auto wait_w = [&](uint32_t b, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
+        };
+        bool ok = true;
+        int g = 0;  // query tiles so far (all items)
+        for (int r = 0; ok; ++r) {
+            const int itm = bwd_item(r);
+            if (itm >= p.n_items) break;
+            const int bh = item_bh(itm), kt = item_kt(itm);
+            const int n_iter = item_iters(kt);
+            for (int it = 0; it < n_iter; ++it, ++g) {
+                ok = wait_w(bar(L::kDQFull), static_cast<uint32_t>(g) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const int q0 = (item_qt0(kt) + it) * kBlockM;
+#pragma unroll
+                for (int pr2 = 0; pr2 < D / 64; ++pr2) {
+                    uint32_t rv[2][32];
+                    tmem_ld32(tmem + lane_off + L::kColDQ + pr2 * 64, rv[0]);
+                    tmem_ld32(tmem + lane_off + L::kColDQ + pr2 * 64 + 32, rv[1]);
+                    tmem_wait_ld();
+                    if (pr2 == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(L::kDQEmpty));
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (lane == 0) bulk_wait_read0();  // the previous reduce has read the buffer
+                        __syncwarp();
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            st_shared_v4(stg + sw128_off(lane, ch), rv[h][4 * ch], rv[h][4 * ch + 1], rv[h][4 * ch + 2],
+                                         rv[h][4 * ch + 3]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_3d(&tm_dqacc, stg, pr2 * 64 + h * 32, q0 + wq * 32, bh);
+                            bulk_commit();
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait0();
+    }
     } else {
-        // ------------------------- math warpgroups: P^T, dS^T, dQ drain, dK/dV
+    regs_inc<L::kRegsMath>();
+    {
+        // ------------------------- math warpgroups: P^T, dS^T, dK/dV
         const int wg = warp >> 2;             // 0: query columns 0-63, 1: 64-127
         const int wq = warp & 3;              // TMEM lane quarter
         const int kr = threadIdx.x & 127;     // key row within the tile == TMEM lane
@@ -494,44 +567,11 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
         const uint64_t alx2 = f2_pack(p.scale, p.scale);
-        const uint32_t stage = sb + L::kStage + (warp & 7) * 4096;
         auto wait_w = [&](uint32_t b, uint32_t parity) {
             return __all_sync(0xffffffffu, mbar_wait(b, parity, p.status));
         };
         bool ok = true;
         int g = 0;  // query tiles processed so far (all items)
-
-        // Drain dQ of query tile `qt` (global tile count gi): this warp's 32
-        // query rows, this warpgroup's half of the d columns, as 32 x 32 FP32
-        // boxes added into the workspace with TMA reduce-add.
-        auto drain_dq = [&](int gi, int qt, int bh) -> bool {
-            if (!wait_w(bar(L::kDQFull), static_cast<uint32_t>(gi) & 1u)) return false;
-            tc_fence_after();
-            const int q0 = qt * kBlockM;
-#pragma unroll
-            for (int cb = 0; cb < D / 64; ++cb) {
-                const int col = wg * (D / 2) + cb * 32;
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + L::kColDQ + col, r);
-                tmem_wait_ld();
-                if (cb == D / 64 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(L::kDQEmpty));
-                }
-                if (lane == 0) bulk_wait_read0();  // this warp's previous reduce has read its box
-                __syncwarp();
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    st_shared_v4(stage + sw128_off(lane, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2], r[4 * ch + 3]);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_reduce_add_3d(&tm_dqacc, stage, col, q0 + wq * 32, bh);
-                    bulk_commit();
-                }
-            }
-            return true;
-        };
 
         for (int r = 0, n = 0; ok; ++r, ++n) {
             const int itm = bwd_item(r);
@@ -544,11 +584,6 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t u = static_cast<uint32_t>(g / QS);
                 const uint32_t cur = static_cast<uint32_t>(g) & 1u;
                 const int qt = qt_begin + it;
-                if (L::kDQAliasS && it >= 1) {
-                    // dQ shares the S^T columns: drain it before the next S^T lands
-                    ok = drain_dq(g - 1, qt - 1, bh);
-                    if (!ok) break;
-                }
                 ok = wait_w(bar(L::kSFull), cur) && wait_w(bar(L::kQFull + s), u & 1u);
                 if (!ok) break;
                 tc_fence_after();
@@ -618,31 +653,25 @@ __global__ void __launch_bounds__(320, 1)
                     fence_async_smem();
                 }
                 mbar_arrive(bar(L::kPFull));
-                if (!L::kDQAliasS && it >= 1) {
-                    // the previous tile's dQ has been computed meanwhile
-                    ok = drain_dq(g - 1, qt - 1, bh);
-                    if (!ok) break;
-                }
                 // dS^T[kr][q] = P * (alpha * dP + (-alpha * delta_q))
                 ok = wait_w(bar(L::kDPFull), cur);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t ds_blk = sb + L::kDSt + wg * 16384;
+                uint32_t dpr[2][32];
+                tmem_ld32(tmem + lane_off + L::kColDP + c0, dpr[0]);
+                tmem_ld32(tmem + lane_off + L::kColDP + c0 + 32, dpr[1]);
+                tmem_wait_ld();  // one wait for both loads
+                tc_fence_before();
+                mbar_arrive(bar(L::kDPEmpty));
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t rr[32];
-                    tmem_ld32(tmem + lane_off + L::kColDP + c0 + h * 32, rr);
-                    tmem_wait_ld();
-                    if (h == 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar(L::kDPEmpty));
-                    }
 #pragma unroll
                     for (int gq = 0; gq < 4; ++gq) {  // 8 queries per group
                         const int c = h * 32 + gq * 8;
                         const float4 na = nd4[c / 4];
                         const float4 nb = nd4[c / 4 + 1];
-                        const uint32_t* rv = &rr[gq * 8];
+                        const uint32_t* rv = &dpr[h][gq * 8];
                         float dv8[8];
                         f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[0]), __uint_as_float(rv[1])), alx2,
                                                 f2_pack(na.x, na.y)),
@@ -668,8 +697,6 @@ __global__ void __launch_bounds__(320, 1)
                 fence_async_smem();
                 mbar_arrive(bar(L::kDSFull));
             }
-            if (!ok) break;
-            ok = drain_dq(g - 1, qt_begin + n_iter - 1, bh);
             if (!ok) break;
             // ------------------------------------------------ dK/dV epilogue
             // Key rows, this warpgroup's half of the d columns: read out of
@@ -717,10 +744,11 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (lane == 0) bulk_wait0();
     }
+    }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == L::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -750,7 +778,7 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
     prof_begin(3, stream);
-    kern<<<grid, 320, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
+    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
     prof_end(3, stream);
     e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -542,14 +542,15 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                 // rescale O after the scores are consumed (keeps register use low)
                 if (j >= 1 && __any_sync(0xffffffffu, changed)) {
                     tc_fence_after();
+                    uint32_t r[D / 32][32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, r[c]);
+                    tmem_wait_ld();  // one wait for all loads
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_tm + c * 32, r);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * rsc);
-                        tmem_st32(o_tm + c * 32, r);
+                        for (int e = 0; e < 32; ++e) r[c][e] = __float_as_uint(__uint_as_float(r[c][e]) * rsc);
+                        tmem_st32(o_tm + c * 32, r[c]);
                     }
                 }
                 tmem_wait_st();  // Pbar (and any rescaled O) written to TMEM
