@@ -758,7 +758,8 @@ template <int D, bool CAUSAL>
 cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     auto kern = bwd_kernel<D, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    static unsigned smem_set = 0;  // devices on which this instantiation's limit is raised
+    cudaError_t e = smem_limit_once(kern, L::kAlloc, &smem_set);
     if (e != cudaSuccess) {
         set_error("bwd_main cudaFuncSetAttribute", e);
         return e;

@@ -672,7 +672,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     constexpr int NQ = kQTilesPerCta<D>;
     using L = FwdLayout<D, MODE, NQ>;
     auto kern = fwd_kernel<D, MODE, CAUSAL, STATS, NQ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    static unsigned smem_set = 0;  // devices on which this instantiation's limit is raised
+    cudaError_t e = smem_limit_once(kern, L::kAlloc, &smem_set);
     if (e != cudaSuccess) {
         set_error("fwd cudaFuncSetAttribute", e);
         return e;

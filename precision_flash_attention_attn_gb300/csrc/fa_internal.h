@@ -71,6 +71,22 @@ void set_error_msg(const char* step, const char* msg);
 void prof_begin(int kind, cudaStream_t stream);
 void prof_end(int kind, cudaStream_t stream);
 
+// Raises a kernel's dynamic shared-memory limit the first time it launches on
+// each device (the setting belongs to the function on that device and stays;
+// repeating the call on every launch only costs host time).  `done` is a
+// per-kernel bit mask of devices already set.
+template <typename Kernel>
+inline cudaError_t smem_limit_once(Kernel kern, int bytes, unsigned* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned bit = (dev >= 0 && dev < 32) ? (1u << dev) : 0u;
+    if (bit && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
+    return e;
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, bool stats, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_pv_err(const StatsArgs& a, cudaStream_t stream);
