@@ -218,8 +218,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
-        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
+        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
         rc = FA_ERR_CUDA;
     if (rc == FA_OK) {
         fa::BwdArgs a{};
@@ -325,8 +325,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
         make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
         make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
-        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
+        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
         return FA_ERR_CUDA;
     fa::BwdArgs a{};
     a.tm_q = &mq;

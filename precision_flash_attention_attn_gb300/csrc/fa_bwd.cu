@@ -25,9 +25,10 @@
 //                    Warp roles: two math warpgroups (warps 0-3: query
 //                    columns 0-63 of the tile, warps 4-7: columns 64-127;
 //                    thread t of a warpgroup owns key row t) recompute P^T and
-//                    dS^T and finally store dK and dV; a drain warpgroup
-//                    (warps 8-11, one TMEM lane quarter each) moves each dQ
-//                    tile from TMEM into the reduce-add, off the math chain;
+//                    dS^T; a drain warpgroup (warps 8-11, one TMEM lane
+//                    quarter each) moves each dQ tile from TMEM into the
+//                    reduce-add and each item's dK and dV from TMEM to HBM
+//                    (TMA stores), off the math chain;
 //                    warp 12 issues TMA loads; warp 13 issues the MMAs.  The
 //                    next tile's S^T and dP^T are issued ahead of the current
 //                    tile's dK/dQ products.
@@ -182,10 +183,6 @@ struct BwdLayout {
     static constexpr int kLse = kStage + 4 * 4096;                // [kQStages][128] FP32 (-LSE*log2e)
     static constexpr int kDelta = kLse + kQStages * 512;          // [kQStages][128] FP32 (-alpha*delta)
     static constexpr int kBar = kDelta + kQStages * 512;
-    // dK/dV epilogue staging (128 key rows, 64-column boxes of 16 KB): the
-    // dS^T buffer holds both at d = 64; at d = 128 dV uses the P^T buffer
-    static constexpr int kEpiDV = kPtInTmem ? kDSt : kPt;
-    static constexpr int kEpiDK = kPtInTmem ? kDSt + kTile : kDSt;
     // barriers
     static constexpr int kKVFull = 0;                         // [kKVBufs]
     static constexpr int kKVEmpty = kKVFull + kKVBufs;        // [kKVBufs]
@@ -202,9 +199,7 @@ struct BwdLayout {
     static constexpr int kDQEmpty = kDQFull + 1;
     static constexpr int kAccDone = kDQEmpty + 1;    // dK, dV of the item complete
     static constexpr int kAccFree = kAccDone + 1;    // dK, dV read out of TMEM
-    static constexpr int kEpiStaged = kAccFree + 1;  // dK, dV rows in the staging buffers
-    static constexpr int kStageFree = kEpiStaged + 1;  // their TMA stores have read them
-    static constexpr int kDrain = kStageFree + 1;
+    static constexpr int kDrain = kAccFree + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kBytes = kTmemSlot + 16;
@@ -292,9 +287,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         mbar_init(bar(L::kDQFull), 1);
         mbar_init(bar(L::kDQEmpty), L::kDrainThreads);
         mbar_init(bar(L::kAccDone), 1);
-        mbar_init(bar(L::kAccFree), L::kMathThreads);
-        mbar_init(bar(L::kEpiStaged), L::kMathThreads);
-        mbar_init(bar(L::kStageFree), 1);
+        mbar_init(bar(L::kAccFree), L::kDrainThreads);
         mbar_init(bar(L::kDrain), 1);
         fence_mbar_init();
     }
@@ -516,7 +509,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         };
         bool ok = true;
         int g = 0;  // query tiles so far (all items)
-        for (int r = 0; ok; ++r) {
+        for (int r = 0, n = 0; ok; ++r, ++n) {
             const int itm = bwd_item(r);
             if (itm >= p.n_items) break;
             const int bh = item_bh(itm), kt = item_kt(itm);
@@ -553,6 +546,45 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     }
                 }
             }
+            if (!ok) break;
+            // -------------------------------------------- dK/dV epilogue
+            // This warp's 32 key rows of dV and dK: read out of TMEM (which
+            // frees the accumulators for the next item's first products),
+            // staged as BF16 in the 128-byte-swizzled box layout (64 columns x
+            // 32 rows, 4 KB) and written by TMA; rows past N are clipped.
+            ok = wait_w(bar(L::kAccDone), static_cast<uint32_t>(n) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+#pragma unroll
+                for (int b64 = 0; b64 < D / 64; ++b64) {
+                    uint32_t av[2][32];
+                    const uint32_t col = (which == 0 ? L::kColDV : L::kColDK) + b64 * 64;
+                    tmem_ld32(tmem + lane_off + col, av[0]);
+                    tmem_ld32(tmem + lane_off + col + 32, av[1]);
+                    tmem_wait_ld();
+                    if (which == 1 && b64 == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(L::kAccFree));
+                    }
+                    if (lane == 0) bulk_wait_read0();  // the previous store or reduce has read the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(stg + sw128_off(lane, ch),
+                                     pack_bf16x2(__uint_as_float(av[ch >> 2][(ch & 3) * 8 + 0]), __uint_as_float(av[ch >> 2][(ch & 3) * 8 + 1])),
+                                     pack_bf16x2(__uint_as_float(av[ch >> 2][(ch & 3) * 8 + 2]), __uint_as_float(av[ch >> 2][(ch & 3) * 8 + 3])),
+                                     pack_bf16x2(__uint_as_float(av[ch >> 2][(ch & 3) * 8 + 4]), __uint_as_float(av[ch >> 2][(ch & 3) * 8 + 5])),
+                                     pack_bf16x2(__uint_as_float(av[ch >> 2][(ch & 3) * 8 + 6]), __uint_as_float(av[ch >> 2][(ch & 3) * 8 + 7])));
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(which == 0 ? &tm_dv : &tm_dk, stg, b64 * 64, kt * kBlockN + wq * 32, bh);
+                        bulk_commit();
+                    }
+                }
+            }
         }
         if (lane == 0) bulk_wait0();
     }
@@ -573,10 +605,10 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         bool ok = true;
         int g = 0;  // query tiles processed so far (all items)
 
-        for (int r = 0, n = 0; ok; ++r, ++n) {
+        for (int r = 0; ok; ++r) {
             const int itm = bwd_item(r);
             if (itm >= p.n_items) break;
-            const int bh = item_bh(itm), kt = item_kt(itm);
+            const int kt = item_kt(itm);
             const int qt_begin = item_qt0(kt);
             const int n_iter = item_iters(kt);
             for (int it = 0; it < n_iter; ++it, ++g) {
@@ -623,15 +655,6 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 }
                 if (g >= 1) {
                     ok = wait_w(bar(L::kPDSFree), static_cast<uint32_t>(g - 1) & 1u);
-                    if (!ok) break;
-                }
-                if (it == 0 && n >= 1) {
-                    // the previous item's dK/dV stores have read the staging buffers
-                    if (threadIdx.x == 0) {
-                        bulk_wait_read0();
-                        mbar_arrive(bar(L::kStageFree));
-                    }
-                    ok = wait_w(bar(L::kStageFree), static_cast<uint32_t>(n - 1) & 1u);
                     if (!ok) break;
                 }
                 if (L::kPtInTmem) {
@@ -697,52 +720,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 fence_async_smem();
                 mbar_arrive(bar(L::kDSFull));
             }
-            if (!ok) break;
-            // ------------------------------------------------ dK/dV epilogue
-            // Key rows, this warpgroup's half of the d columns: read out of
-            // TMEM (which frees the accumulators for the next item), staged as
-            // BF16 in 128-byte-swizzled 64-column boxes, written by TMA (rows
-            // past N are clipped).
-            ok = wait_w(bar(L::kAccDone), static_cast<uint32_t>(n) & 1u);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t acc[2][D / 2];
-#pragma unroll
-            for (int which = 0; which < 2; ++which)
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tmem_ld32(tmem + lane_off + (which == 0 ? L::kColDV : L::kColDK) + wg * (D / 2) + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&acc[which][c * 32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(L::kAccFree));
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t base = sb + (which == 0 ? L::kEpiDV : L::kEpiDK);
-#pragma unroll
-                for (int c = 0; c < D / 2; c += 8) {
-                    const int col = wg * (D / 2) + c;  // column within the d columns
-                    st_shared_v4(base + (col >> 6) * 16384 + sw128_off(kr, (col & 63) >> 3),
-                                 pack_bf16x2(__uint_as_float(acc[which][c]), __uint_as_float(acc[which][c + 1])),
-                                 pack_bf16x2(__uint_as_float(acc[which][c + 2]), __uint_as_float(acc[which][c + 3])),
-                                 pack_bf16x2(__uint_as_float(acc[which][c + 4]), __uint_as_float(acc[which][c + 5])),
-                                 pack_bf16x2(__uint_as_float(acc[which][c + 6]), __uint_as_float(acc[which][c + 7])));
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(bar(L::kEpiStaged));
-            if (threadIdx.x == 0) {
-                ok = mbar_wait(bar(L::kEpiStaged), static_cast<uint32_t>(n) & 1u, p.status);
-                if (ok) {
-                    for (int b = 0; b < D / 64; ++b) {
-                        tma_store_3d(&tm_dv, sb + L::kEpiDV + b * 16384, b * 64, kt * kBlockN, bh);
-                        tma_store_3d(&tm_dk, sb + L::kEpiDK + b * 16384, b * 64, kt * kBlockN, bh);
-                    }
-                    bulk_commit();
-                }
-            }
         }
-        if (lane == 0) bulk_wait0();
     }
     }
 

@@ -35,7 +35,7 @@ struct BwdArgs {
     const CUtensorMap* tm_v;
     const CUtensorMap* tm_do;
     const CUtensorMap* tm_dqacc;  // FP32 [BH, N, d] accumulator (reduce-add target)
-    const CUtensorMap* tm_dk;     // dK, dV as TMA store targets (BF16 [BH, N, d])
+    const CUtensorMap* tm_dk;     // dK, dV as TMA store targets (BF16 [BH, N, d], 64 x 32 boxes)
     const CUtensorMap* tm_dv;
     const void* o;                // [BH, N, d] BF16 or FP32 (mode 2)
     const float* lse;             // [BH, N]
