@@ -75,6 +75,26 @@ def test_gpt2s_full_size_sampled(fa, mode):
         assert rel_fro(dv.reshape(BH, c.N, c.d)[h, rows], ex["dv"]) <= GRAD_REL_TOL
 
 
+@pytest.mark.parametrize("name,mode", [("gpt2m", 0), ("long", 1), ("ties", 2)])
+def test_other_workloads_full_size_sampled(fa, name, mode):
+    # The remaining workloads at their full sizes (gradients of all heads
+    # computed on the GPU; one head's sampled rows checked against the oracle,
+    # which recomputes that head's LSE and delta itself).
+    c = case(name)
+    dq, dk, dv = _run(fa, c, mode)
+    qf, kf, vf, gf = _arrays(c)
+    BH = c.B * c.H
+    h = (BH * 2) // 3
+    rng = np.random.default_rng(200 + mode)
+    rows = np.unique(np.concatenate([rng.choice(c.N, 48, replace=False), [0, 127, 128, c.N - 1]]))
+    sl = slice(h, h + 1)
+    ex = orc.bwd(qf[sl], kf[sl], vf[sl], gf[sl], c.causal, c.scale, q_rows=rows, k_rows=rows)
+    floor = 1e-3 * max(np.linalg.norm(ex[n]) for n in ("dq", "dk", "dv"))
+    assert rel_fro(dq.reshape(BH, c.N, c.d)[h, rows], ex["dq"], floor) <= GRAD_REL_TOL
+    assert rel_fro(dk.reshape(BH, c.N, c.d)[h, rows], ex["dk"], floor) <= GRAD_REL_TOL
+    assert rel_fro(dv.reshape(BH, c.N, c.d)[h, rows], ex["dv"], floor) <= GRAD_REL_TOL
+
+
 def test_causal_mask_bit_exact_dk_dv(fa):
     c = case("tiny")
     i0 = 60

@@ -75,6 +75,19 @@ def test_gpt2s_full_size_sampled_rows(fa, mode):
     _check(c, o, lse, mode, rows=rows)
 
 
+@pytest.mark.parametrize("name,mode", [("gpt2m", 0), ("gpt2m", 1), ("long", 0), ("long", 2), ("ties", 1), ("ties", 2)])
+def test_other_workloads_full_size_sampled_rows(fa, name, mode):
+    # The remaining workloads at their full sizes, in the launch configuration
+    # the benchmark uses (persistent grid, many items per CTA): sampled rows
+    # against the oracle, planted tie rows among them.
+    c = case(name)
+    o, lse = _run(fa, c, mode)
+    BH = c.B * c.H
+    planted = np.flatnonzero(c.planted.reshape(-1))
+    rows = sample_rows(BH, c.N, 256, seed=17 + mode, must=planted[:: max(1, len(planted) // 32)])
+    _check(c, o, lse, mode, rows=rows)
+
+
 def test_causal_mask_bit_exact(fa):
     c = case("tiny")
     q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
