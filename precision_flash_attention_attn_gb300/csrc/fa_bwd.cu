@@ -55,9 +55,24 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     constexpr int kUnroll = 4;
     const int lane = threadIdx.x & 31;
     const int sub = lane % TPR;
+    // The first half of the blocks compute the rows, the second half clear the
+    // dQ accumulator, so reads and writes proceed side by side.
+    const int row_blocks = static_cast<int>(gridDim.x) / 2;
+    if (static_cast<int>(blockIdx.x) >= row_blocks) {
+        const size_t n4 = static_cast<size_t>(a.BH) * a.N * D / 4;
+        float4* acc4 = reinterpret_cast<float4*>(a.dq_acc);
+        const size_t nthr = static_cast<size_t>(gridDim.x - row_blocks) * blockDim.x;
+        const size_t tid = static_cast<size_t>(blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
+        for (size_t e = tid; e < n4; e += 4 * nthr) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e + u * nthr < n4) acc4[e + u * nthr] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
+    }
     // rows < 2^31 (BH * Npad * d is checked against it), so 32-bit index math
     const int rows = a.BH * a.Npad;
-    const int nwarps = static_cast<int>(gridDim.x) * (blockDim.x >> 5);
+    const int nwarps = row_blocks * (blockDim.x >> 5);
     const int gw = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
     for (int r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
@@ -116,16 +131,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
                 a.lse2[r[u]] = valid[u] ? -a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : -INFINITY;
             }
         }
-    }
-    // zero the dQ accumulator, four 16-byte stores per thread and pass
-    const size_t n4 = static_cast<size_t>(a.BH) * a.N * D / 4;
-    float4* acc4 = reinterpret_cast<float4*>(a.dq_acc);
-    const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
-    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (size_t e = tid; e < n4; e += 4 * nthr) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (e + u * nthr < n4) acc4[e + u * nthr] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
