@@ -370,69 +370,85 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         };
         bool ok = true;
         bool issued = false;
+        // S^T(gi) = K Q^T with the K tile at sK
+        auto issue_s = [&](int gi, uint32_t sK) {
+            const int s = gi % QS;
+            ok = ok && wait_all(bar(L::kQFull + s), static_cast<uint32_t>(gi / QS) & 1u);
+            if (ok && gi >= 1) ok = wait_all(bar(L::kSEmpty), static_cast<uint32_t>(gi - 1) & 1u);
+            if (ok && gi >= 1 && L::kDQAliasS) ok = wait_all(bar(L::kDQEmpty), static_cast<uint32_t>(gi - 1) & 1u);
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t sQ = sb + L::kQ + s * L::kTile;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + L::kColS, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ + ko, 16, 1024),
+                                kIdSS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(L::kSFull));
+            }
+            __syncwarp();
+            issued = true;
+        };
+        // dP^T(gi) = V dO^T with the V tile at sV (Q/dO stage gi is already known to be loaded)
+        auto issue_dp = [&](int gi, uint32_t sV) {
+            const int s = gi % QS;
+            if (ok && gi >= 1) ok = wait_all(bar(L::kDPEmpty), static_cast<uint32_t>(gi - 1) & 1u);
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t sDO = sb + L::kDO + s * L::kTile;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sDO + ko, 16, 1024),
+                                kIdSS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(L::kDPFull));
+            }
+            __syncwarp();
+        };
+        // Software pipeline: the next tile's S^T is issued as soon as the math
+        // warps have read this tile's S^T, and the next dP^T as soon as they
+        // have read this dP^T, so both are ready before the math warps ask.
+        // The next tile may belong to the next item (its K/V sit in the other
+        // buffer), so items follow one another without a bubble.  With dQ
+        // aliasing S^T (d = 128, one K/V buffer) the next S^T must instead wait
+        // for this tile's dQ to be drained, after the dQ product, and a new
+        // item starts only after the previous one's products.
         int g = 0;  // query tiles processed so far (all items)
-        for (int r = 0, n = 0; ok; ++r, ++n) {
-            const int itm = bwd_item(r);
-            if (itm >= p.n_items) break;
+        int itm = bwd_item(0);
+        bool head_issued = false;  // this item's first S^T/dP^T already issued
+        for (int r = 0, n = 0; ok && itm < p.n_items; ++r, ++n) {
             const int kt = item_kt(itm);
             const int n_iter = item_iters(kt);
             const int kb = n % KVB;
             const uint32_t sK = sb + L::kK + kb * L::kTile;
             const uint32_t sV = sb + L::kV + kb * L::kTile;
-            ok = wait_all(bar(L::kKVFull + kb), static_cast<uint32_t>(n / KVB) & 1u);
-            if (!ok) break;
-            // S^T(gi) = K Q^T
-            auto issue_s = [&](int gi) {
-                const int s = gi % QS;
-                ok = ok && wait_all(bar(L::kQFull + s), static_cast<uint32_t>(gi / QS) & 1u);
-                if (ok && gi >= 1) ok = wait_all(bar(L::kSEmpty), static_cast<uint32_t>(gi - 1) & 1u);
-                if (ok && gi >= 1 && L::kDQAliasS) ok = wait_all(bar(L::kDQEmpty), static_cast<uint32_t>(gi - 1) & 1u);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t sQ = sb + L::kQ + s * L::kTile;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16_ss(tmem + L::kColS, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ + ko, 16, 1024),
-                                    kIdSS, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(L::kSFull));
-                }
-                __syncwarp();
-                issued = true;
-            };
-            // dP^T(gi) = V dO^T   (Q/dO stage gi is already known to be loaded)
-            auto issue_dp = [&](int gi) {
-                const int s = gi % QS;
-                if (ok && gi >= 1) ok = wait_all(bar(L::kDPEmpty), static_cast<uint32_t>(gi - 1) & 1u);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t sDO = sb + L::kDO + s * L::kTile;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16_ss(tmem + L::kColDP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sDO + ko, 16, 1024),
-                                    kIdSS, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(L::kDPFull));
-                }
-                __syncwarp();
-            };
-            // Software pipeline: the next tile's S^T is issued as soon as the math
-            // warps have read this tile's S^T, and the next dP^T as soon as they
-            // have read this dP^T, so both are ready before the math warps ask.
-            // With dQ aliasing S^T (d = 128) the next S^T must instead wait for
-            // this tile's dQ to be drained, after the dQ product.
-            issue_s(g);
-            issue_dp(g);
+            const int itm_next = bwd_item(r + 1);
+            const bool has_next = itm_next < p.n_items;
+            const uint32_t sK_next = sb + L::kK + ((n + 1) % KVB) * L::kTile;
+            const uint32_t sV_next = sb + L::kV + ((n + 1) % KVB) * L::kTile;
+            if (!head_issued) {
+                ok = wait_all(bar(L::kKVFull + kb), static_cast<uint32_t>(n / KVB) & 1u);
+                if (!ok) break;
+                issue_s(g, sK);
+                issue_dp(g, sV);
+            }
+            head_issued = false;
             for (int it = 0; it < n_iter && ok; ++it, ++g) {
                 const int s = g % QS;
                 const uint32_t cur = static_cast<uint32_t>(g) & 1u;
                 const uint32_t sQ = sb + L::kQ + s * L::kTile;
                 const uint32_t sDO = sb + L::kDO + s * L::kTile;
-                if (!L::kDQAliasS && it + 1 < n_iter) issue_s(g + 1);
+                const bool last = (it + 1 == n_iter);
+                // the next tile (of this item, or the next item's first)
+                const bool ahead = !L::kDQAliasS && (!last || has_next);
+                if (ahead) {
+                    if (last) ok = wait_all(bar(L::kKVFull + (n + 1) % KVB), static_cast<uint32_t>((n + 1) / KVB) & 1u);
+                    issue_s(g + 1, last ? sK_next : sK);
+                }
                 // dV += P^T dO; the item's first product overwrites dV, which
                 // the previous item's epilogue must have read out
                 ok = ok && wait_all(bar(L::kPFull), cur);
@@ -452,7 +468,10 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (!L::kDQAliasS && it + 1 < n_iter) issue_dp(g + 1);
+                if (ahead) {
+                    issue_dp(g + 1, last ? sV_next : sV);
+                    if (last) head_issued = true;
+                }
                 if (!ok) break;
                 // dK += dS^T Q
                 ok = wait_all(bar(L::kDSFull), cur);
@@ -481,17 +500,18 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     mma_commit(bar(L::kDQFull));
                     mma_commit(bar(L::kQEmpty + s));
                     mma_commit(bar(L::kPDSFree));
-                    if (it + 1 == n_iter) {
+                    if (last) {
                         mma_commit(bar(L::kKVEmpty + kb));  // last read of this item's K and V
                         mma_commit(bar(L::kAccDone));
                     }
                 }
                 __syncwarp();
-                if (L::kDQAliasS && it + 1 < n_iter) {
-                    issue_s(g + 1);
-                    issue_dp(g + 1);
+                if (L::kDQAliasS && !last) {
+                    issue_s(g + 1, sK);
+                    issue_dp(g + 1, sV);
                 }
             }
+            itm = itm_next;
         }
         // Drain: every MMA this warp issued has completed before TMEM is freed.
         if (issued) {
