@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
             const int q0 = tile_q0(cq, t);
             const int qrow = q0 + row;
             float M = -INFINITY;  // running max of raw scores
-            int C = 0;            // running count of keys equal to M
+            int C = 0;            // running count of keys equal to M (only C > 1 kept outside statistics)
             float m = -INFINITY;  // current shift, raw units
             float mc = -INFINITY; // m * sl2
             float l = 0.f;
@@ -445,10 +445,49 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                         for (int e = 0; e < 8; ++e) mx[e] = fmax3(mx[e], s[c + e], s[c + 8 + e]);
                     tm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 }
-                if (MODE == 1 || STATS) {
-                    // The tile's tie count matters only where the tile max reaches
-                    // the running max; warps where no row does skip the count (the
-                    // common case once the max has settled).
+                if (MODE == 1 && !STATS) {
+                    // Only C > 1 matters here.  A tile max equal to the running
+                    // max adds at least one tie to the C >= 1 already counted, so
+                    // C > 1 follows without a count; only a new running max needs
+                    // the tile's own count.  For 2^-76 <= |tm| <= 2^27 the non-tie
+                    // indicator is one saturated FMA per key: (tm - s) * 2^100 is
+                    // 0 exactly at a tie and at least 1 otherwise, because the
+                    // nearest FP32 value below tm lies at least 2^-100 away and
+                    // tm * 2^100 is exact.  Other maxima take the compare loop.
+                    const bool newmax = tm > M;
+                    const bool same = tm == M;
+                    if (__any_sync(0xffffffffu, newmax)) {
+                        int tc;
+                        const float atm = fabsf(tm);
+                        const bool in_range = !newmax || (atm >= 0x1p-76f && atm <= 0x1p27f);
+                        if (__all_sync(0xffffffffu, in_range)) {
+                            const float tb = tm * 0x1p100f;
+                            uint64_t nt2[4] = {0ull, 0ull, 0ull, 0ull};  // non-tie counts, as 4 pairs
+#pragma unroll
+                            for (int e = 0; e < kBlockN / 2; ++e)
+                                nt2[e & 3] = f2_add(nt2[e & 3], f2_pack(fma_sat(s[2 * e], -0x1p100f, tb),
+                                                                        fma_sat(s[2 * e + 1], -0x1p100f, tb)));
+                            float n0, n1;
+                            f2_unpack(f2_add(f2_add(nt2[0], nt2[1]), f2_add(nt2[2], nt2[3])), n0, n1);
+                            tc = kBlockN - static_cast<int>(n0 + n1);
+                        } else {
+                            int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                            for (int c = 0; c < kBlockN; c += 8)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
+                            tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
+                        }
+                        if (newmax) {
+                            M = tm;
+                            C = tc;
+                        }
+                    }
+                    if (same) C = 2;
+                } else if (STATS) {
+                    // Exact running tie count (reported per row).  The tile's count
+                    // matters only where the tile max reaches the running max; warps
+                    // where no row does skip it.
                     int tc = 0;
                     if (__any_sync(0xffffffffu, tm >= M)) {
                         int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};

@@ -121,3 +121,32 @@ def test_identical_keys_give_identical_scores(fa):
                               fa.attention_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), False, 0.125, 0)[0],
                               False, 0.125, 0)
     assert np.all(tc.cpu().numpy() == N)
+
+
+def test_stabilised_tie_decisions_agree_across_score_magnitudes(fa):
+    # Ternary Q, K times 2^a give integer scores times 2^(2a), and the scale
+    # 2^(-2a)/4 maps all three to the same logits.  Every FP32 product in the
+    # kernel then differs only by an exact power of two, so the outputs are
+    # bit-identical exactly when the tie decisions agree.  Row maxima near
+    # 1 (a = 0) take the saturated-FMA count; those below 2^-76 (a = -42) or
+    # above 2^27 (a = 14) take the compare loop.  Each is also checked
+    # against the oracle, and mode 1 must differ from mode 0.
+    from types import SimpleNamespace
+    from precision_flash_attention_attn_gb300.inputs import bf16_bits
+    rng = np.random.default_rng(31)
+    B, H, N, d = 1, 4, 384, 64
+    tq = rng.integers(-1, 2, (B, H, N, d)).astype(np.float32)
+    tk = rng.integers(-1, 2, (B, H, N, d)).astype(np.float32)
+    v = bf16_bits(rng.standard_normal((B, H, N, d)).astype(np.float32))
+    outs = {}
+    for a in (-42, 0, 14):
+        c = SimpleNamespace(B=B, H=H, N=N, d=d, causal=True, scale=2.0 ** (-2 * a) / 4,
+                            q=bf16_bits(tq * np.float32(2.0 ** a)), k=bf16_bits(tk * np.float32(2.0 ** a)), v=v)
+        for mode in (0, 1):
+            o, lse = _run(fa, c, mode)
+            _check(c, o, lse, mode)
+            outs[(a, mode)] = o
+    for mode in (0, 1):
+        assert np.array_equal(outs[(0, mode)], outs[(-42, mode)]), mode
+        assert np.array_equal(outs[(0, mode)], outs[(14, mode)]), mode
+    assert not np.array_equal(outs[(0, 0)], outs[(0, 1)])
