@@ -6,7 +6,10 @@ on the GPT-2-small attention training shape (B=8, H=12, N=1024, d=64, causal,
 scale 1/8; seeded synthetic BF16 inputs with 5% planted tied-max rows).
 Throughput counts 12*d algorithmic FLOP per visible (query, key) pair per mode
 (4d forward: QK^T and PV; 8d backward: dP, dV, dK, dQ; the backward's
-recomputation of S is not counted).
+recomputation of S is not counted).  The timed steps run as one launch of a
+CUDA graph captured from the fa_fwd / fa_bwd_noalloc calls (the L2 flush and
+the step and mode events are graph nodes too); the end-to-end figure runs
+fa_fwd / fa_bwd call by call with the host copies.
 
 Prints one JSON line.  ``--impl reference`` times the CPU FP64 oracle instead
 (the only reference implementation of this method available), on a bounded
@@ -276,21 +279,58 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2x the 129 MB L2
 
-    def one_mode(m, qq=q, kk=k, vv=v, gg=do):
+    def one_mode(m, qq=q, kk=k, vv=v, gg=do, st=stream, bwd=fa.fa_bwd):
         b = outs[m]
-        fa.fa_fwd(qq, kk, vv, b["o"], b["lse"], B, H, N, d, causal, scale, m, stream)
-        fa.fa_bwd(qq, kk, vv, b["o"], b["lse"], gg, b["dq"], b["dk"], b["dv"], B, H, N, d, causal, scale, m,
-                  stream)
+        fa.fa_fwd(qq, kk, vv, b["o"], b["lse"], B, H, N, d, causal, scale, m, st)
+        bwd(qq, kk, vv, b["o"], b["lse"], gg, b["dq"], b["dk"], b["dv"], B, H, N, d, causal, scale, m, st)
 
     for _ in range(args.warmup):
         flush.zero_()
         for _, m in MODES:
-            one_mode(m)
+            one_mode(m, bwd=fa.fa_bwd_noalloc)
     torch.cuda.synchronize()
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel timeout during warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(MODES) + 1)] for _ in range(args.steps)]
+    # The K timed steps are captured, with the L2 flush between steps and an
+    # event at every mode boundary, into one CUDA graph that is launched once:
+    # a step enqueued call by call costs more host time than its GPU time.
+    # An event-record node between two kernels costs about 3 us, so the
+    # per-kernel events (library profiling) go into a second graph of the same
+    # K steps, launched once right after; it gives the per-kernel durations.
+    # Where capture is unavailable the steps are launched call by call.
+    def capture(kernel_events):
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(MODES) + 1)]
+               for _ in range(args.steps)]
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        if kernel_events:
+            fa.fa_profile_start()
+        try:
+            with torch.cuda.graph(g, stream=cap):
+                for s in range(args.steps):
+                    flush.zero_()
+                    evs[s][0].record(cap)
+                    for i, (_, m) in enumerate(MODES):
+                        one_mode(m, st=cap, bwd=fa.fa_bwd_noalloc)
+                        evs[s][i + 1].record(cap)
+        except Exception:
+            if kernel_events:
+                fa.fa_profile_stop()
+            raise
+        return g, evs
+
+    graph = graph_k = None
+    timing = (f"one CUDA graph launch of the {args.steps} steps (captured fa_fwd + fa_bwd_noalloc calls); "
+              "per-kernel durations from a second launch with an event pair per kernel")
+    try:
+        graph, ev = capture(False)
+        graph_k, _ = capture(True)          # its profiling session stays open until after its launch
+    except Exception as exc:  # noqa: BLE001 - any capture failure falls back to eager launches
+        graph = graph_k = None
+        timing = f"eager launches (graph capture unavailable: {type(exc).__name__})"
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(MODES) + 1)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
     gpu_index = None
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [x for x in cvd.split(",") if x.strip()]
@@ -301,17 +341,28 @@ def run_ours(args):
     sampler = ClockSampler(gpu_index)
     sampler.start()
     time.sleep(0.3)
-    fa.fa_profile_start()
+    if graph is None:
+        fa.fa_profile_start()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    for s in range(args.steps):
-        flush.zero_()                       # L2 flushed between steps, outside the events
-        e = ev[s]
-        e[0].record(stream)
-        for i, (_, m) in enumerate(MODES):
-            one_mode(m)
-            e[i + 1].record(stream)
+    if graph is not None:
+        for _, m in MODES:                  # every output must come from the graph launch
+            for kname in ("dq", "dk", "dv"):
+                outs[m][kname].fill_(float("nan"))
+        graph.replay()
+        wrote = all(bool(torch.isfinite(outs[m][kname]).all()) for _, m in MODES for kname in ("dq", "dk", "dv"))
+        if not wrote:
+            raise RuntimeError("the graph launch left gradient buffers unwritten")
+        graph_k.replay()                    # the same K steps with an event pair per kernel
+    else:
+        for s in range(args.steps):
+            flush.zero_()                       # L2 flushed between steps, outside the events
+            e = ev[s]
+            e[0].record(stream)
+            for i, (_, m) in enumerate(MODES):
+                one_mode(m, bwd=fa.fa_bwd_noalloc)
+                e[i + 1].record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -384,7 +435,8 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
                    "modes": [n for n, _ in MODES], "planted_tie_rows": 0.05,
                    "flop_per_step": flop_step, "flop_convention": "12*d per visible pair per mode",
-                   "l2": "flushed between steps (256 MiB write, outside the timed events)"},
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "timing": timing},
         "frac_of_peak": value / world / float(peaks["bf16_tflops"]),
         "peak_source": f"bf16_tflops {peaks['bf16_tflops']} ({peak_src})",
         "per_mode": {n: {"ms": per_mode_ms[i] / args.steps,

@@ -167,7 +167,10 @@ int fa_device_status(fa_stream_t stream, int reset);
  * lazily and reused; at most FA_PROFILE_MAX_LAUNCHES launches are recorded per
  * session (later ones are counted in launches[] but not timed, and
  * fa_profile_stop returns FA_ERR_ALLOC).  Not thread-safe across concurrent
- * callers.
+ * callers.  Launches captured into a CUDA graph during a session record their
+ * events as external event-record nodes (cudaEventRecordExternal): launch the
+ * instantiated graph once, then stop the session, and the totals are that
+ * launch's.
  */
 enum {
     FA_KERNEL_FWD = 0,       /* forward (modes 0-2) */

@@ -1,7 +1,9 @@
 // Per-kernel CUDA-event timing behind fa_profile_start / fa_profile_stop.
 // While a session is active every launch site brackets its kernel with two
 // events recorded on the launch stream; stopping synchronises them and sums
-// the durations per kernel kind.
+// the durations per kernel kind.  On a stream that is being captured into a
+// CUDA graph the two events become event-record nodes of the graph, so the
+// durations are those of the graph's launch.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,6 +28,15 @@ std::vector<cudaEvent_t> g_pool;
 std::vector<Record> g_records;
 long long g_launches[FA_KERNEL_COUNT];
 
+// Records e on s; while s is being captured, as an external event-record node
+// (a plain record there would only order the capture).
+cudaError_t record(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    return cudaEventRecord(e, s);
+}
+
 bool ensure_pool(size_t n) {
     while (g_pool.size() < n) {
         cudaEvent_t e;
@@ -49,7 +60,7 @@ void prof_begin(int kind, cudaStream_t stream) {
         g_overflow = true;
         return;
     }
-    if (cudaEventRecord(g_pool[2 * i], stream) != cudaSuccess) {
+    if (record(g_pool[2 * i], stream) != cudaSuccess) {
         g_overflow = true;
         return;
     }
@@ -61,7 +72,7 @@ void prof_end(int kind, cudaStream_t stream) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_active || !g_pending || kind != g_pending_kind) return;
     const size_t i = g_records.size();
-    if (cudaEventRecord(g_pool[2 * i + 1], stream) != cudaSuccess) {
+    if (record(g_pool[2 * i + 1], stream) != cudaSuccess) {
         g_overflow = true;
         g_pending = false;
         return;
