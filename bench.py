@@ -320,14 +320,16 @@ def run_ours(args):
             raise
         return g, evs
 
-    graph = graph_k = None
+    graph = graph_k = ev_k = None
     timing = (f"one CUDA graph launch of the {args.steps} steps (captured fa_fwd + fa_bwd_noalloc calls); "
               "per-kernel durations from a second launch with an event pair per kernel")
     try:
         graph, ev = capture(False)
-        graph_k, _ = capture(True)          # its profiling session stays open until after its launch
+        # its profiling session stays open until after its launch; the graph's
+        # event-record nodes need their events alive as long as the graph
+        graph_k, ev_k = capture(True)
     except Exception as exc:  # noqa: BLE001 - any capture failure falls back to eager launches
-        graph = graph_k = None
+        graph = graph_k = ev_k = None
         timing = f"eager launches (graph capture unavailable: {type(exc).__name__})"
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(MODES) + 1)] for _ in range(args.steps)]
     torch.cuda.synchronize()
@@ -375,6 +377,7 @@ def run_ours(args):
     for e in ev:
         for i in range(len(MODES)):
             per_mode_ms[i] += e[i].elapsed_time(e[i + 1])
+    graph = graph_k = None                  # release the graphs before the events they record
     total_ms = max_over_ranks(sum(per_mode_ms), dist, dev)
     ms_step = total_ms / args.steps
     value = world * flop_step * args.steps / (total_ms * 1e-3) / 1e12
@@ -391,6 +394,9 @@ def run_ours(args):
     e2e_steps = max(3, args.steps // 4)
     if dist is not None:
         dist.barrier()
+    # Each mode's outputs go to the host on a copy stream while the next mode
+    # computes; the step ends when the last copy has landed.
+    copy_stream = torch.cuda.Stream()
     for s in range(e2e_steps + 2):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -399,8 +405,13 @@ def run_ours(args):
             dq_in[n].view(torch.int16).copy_(pin[n], non_blocking=True)
         for _, m in MODES:
             one_mode(m, dq_in["q"], dq_in["k"], dq_in["v"], dq_in["do"])
-            for kname, t in outs[m].items():
-                host_out[m][kname].copy_(t, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                for kname, t in outs[m].items():
+                    host_out[m][kname].copy_(t, non_blocking=True)
+        stream.wait_stream(copy_stream)
         b.record(stream)
         b.synchronize()
         if s >= 2:
