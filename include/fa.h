@@ -11,7 +11,8 @@
  *                       rm = rowmax(S) and rs = number of keys whose raw score
  *                       equals rm exactly, the shift is beta*rm if rm > 0 and
  *                       rs > 1, 0 if rm < 0 and rs > 1, rm otherwise (beta = 2,
- *                       the value of the paper's Figure 7 runs); O stored BF16.
+ *                       the value of the paper's Figure 7 runs, unless
+ *                       fa_fwd_ex / fa_tie_stats_ex set another); O stored BF16.
  *                       The result equals the baseline's in exact arithmetic.
  *   FA_MODE_FP32_OUT    as the baseline, but O is stored in FP32 (the
  *                       "compute O in FP32 in the forward" isolation
@@ -82,6 +83,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            fa_stream_t stream);
 
 /*
+ * Parameters of the stabilised softmax (mode 1; section 3.4.5, "The modified
+ * safe softmax"):
+ *   beta : the shift factor of rows with a positive, repeated maximum
+ *          (m = beta*rm).  The section requires beta > 1 and names [2, 8] as
+ *          the range the authors use; beta = 2 is the value of its Figure 7
+ *          runs.  Finite values > 1 are accepted.  A large beta on a row with
+ *          a large positive repeated maximum underflows every Pbar of that row
+ *          (exp(-(beta-1)*scale*rm) below the FP32 range), and O then is not
+ *          finite; the section restricts the rule to rows where the plain
+ *          softmax is stable.
+ *   eps  : the tolerance of the tie test rm - S <= eps.  Only eps = 0, exact
+ *          ties of the FP32 raw scores, is supported (FA_ERR_UNSUPPORTED
+ *          otherwise): in a single tiled pass a key counted within eps of a
+ *          running maximum may fall out of range when a later tile raises the
+ *          maximum, so eps > 0 needs the whole row first.
+ * A NULL pointer selects the defaults (beta = FA_STAB_BETA_DEFAULT, eps = 0).
+ * Modes 0 and 2 check the parameters but do not use them.
+ */
+typedef struct {
+    float beta;
+    float eps;
+} fa_stab_params_t;
+#define FA_STAB_BETA_DEFAULT 2.0f
+
+/*
+ * fa_fwd_ex -- fa_fwd with explicit stabilised-softmax parameters.
+ * FA_ERR_INVALID_ARG if beta is not a finite value > 1 or eps is negative or
+ * not finite; FA_ERR_UNSUPPORTED if eps > 0.  Otherwise as fa_fwd.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int d, int causal, float scale, int mode,
+              const fa_stab_params_t* params, fa_stream_t stream);
+
+/*
  * fa_bwd -- attention backward from the saved LSE (P is recomputed as
  * exp(S - LSE)); delta = rowsum(dO o O) uses the stored o of the same mode
  * (BF16 in modes 0/1, FP32 in mode 2), dP = dO V^T, dS = scale * P o (dP -
@@ -147,6 +182,17 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o,
                  int B, int H, int N, int d, int causal, float scale, int mode,
                  int32_t* tie_count, float* pv_err, int32_t* p_one,
                  fa_stream_t stream);
+
+/*
+ * fa_tie_stats_ex -- fa_tie_stats with explicit stabilised-softmax parameters
+ * (checked as by fa_fwd_ex).  The p_one counts of mode 1 follow beta; o must
+ * come from fa_fwd_ex with the same parameters.
+ */
+int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o,
+                    int B, int H, int N, int d, int causal, float scale, int mode,
+                    const fa_stab_params_t* params,
+                    int32_t* tie_count, float* pv_err, int32_t* p_one,
+                    fa_stream_t stream);
 
 /*
  * fa_device_status -- synchronises `stream`, then returns FA_ERR_TIMEOUT if any

@@ -114,6 +114,19 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     return FA_OK;
 }
 
+// Stabilised-softmax parameters (NULL: the defaults).  "The modified safe
+// softmax" of section 3.4.5 requires beta > 1; only exact ties (eps = 0) are
+// supported by the one-pass tiled forward.
+int check_params(const fa_stab_params_t* prm, float* beta) {
+    *beta = FA_STAB_BETA_DEFAULT;
+    if (!prm) return FA_OK;
+    if (!std::isfinite(prm->beta) || !(prm->beta > 1.f)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(prm->eps) || prm->eps < 0.f) return FA_ERR_INVALID_ARG;
+    if (prm->eps != 0.f) return FA_ERR_UNSUPPORTED;
+    *beta = prm->beta;
+    return FA_OK;
+}
+
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
 }  // namespace
@@ -146,10 +159,17 @@ const char* fa_status_string(int status) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            int causal, float scale, int mode, fa_stream_t stream) {
+    return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, mode, nullptr, stream);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              int causal, float scale, int mode, const fa_stab_params_t* params, fa_stream_t stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
+    float beta = 0.f;
+    if ((rc = check_params(params, &beta))) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
@@ -176,6 +196,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     a.mode = mode;
     a.scale = scale;
     a.scale_log2 = log2e_times(scale);
+    a.beta = beta;
     a.status = di->status;
     a.num_sms = di->num_sms;
     return fa::launch_fwd(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -361,11 +382,20 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
                  int causal, float scale, int mode, int32_t* tie_count, float* pv_err, int32_t* p_one,
                  fa_stream_t stream) {
+    return fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, nullptr, tie_count, pv_err, p_one,
+                           stream);
+}
+
+int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
+                    int causal, float scale, int mode, const fa_stab_params_t* params, int32_t* tie_count,
+                    float* pv_err, int32_t* p_one, fa_stream_t stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tie_count) ||
         !aligned16(pv_err) || (p_one && !aligned16(p_one)))
         return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
+    float beta = 0.f;
+    if ((rc = check_params(params, &beta))) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
@@ -384,6 +414,7 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int
     a.lse = nullptr;
     a.tie_count = tie_count;
     a.p_one = p_one;
+    a.beta = beta;
     a.BH = BH;
     a.N = N;
     a.d = d;

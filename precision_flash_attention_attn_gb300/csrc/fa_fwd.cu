@@ -113,6 +113,7 @@ struct FwdParams {
     int n_cq;     // query-tile groups (of NQ tiles) per (batch, head)
     int n_items;  // BH * n_cq work items
     float scale_log2;
+    float beta;   // mode 1: shift factor of rows with a positive repeated maximum
     int* status;
 };
 
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                 }
                 float m_new = M;
                 if (MODE == 1 && C > 1) {
-                    if (M > 0.f) m_new = kStabBeta * M;
+                    if (M > 0.f) m_new = p.beta * M;
                     else if (M < 0.f) m_new = 0.f;
                 }
                 const float mc_new = m_new * sl2;
@@ -725,6 +726,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.BH = a.BH;
     p.N = a.N;
     p.scale_log2 = a.scale_log2;
+    p.beta = a.beta;
     p.status = a.status;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
     p.n_cq = (n_qt + NQ - 1) / NQ;

@@ -10,8 +10,6 @@ namespace fa {
 constexpr int kBlockM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBlockN = 128;  // keys per tile
 
-// Stabilised-softmax constant beta (the paper's Figure 7 runs use beta = 2).
-constexpr float kStabBeta = 2.0f;
 
 struct FwdArgs {
     const CUtensorMap* tm_q;
@@ -25,6 +23,7 @@ struct FwdArgs {
     int BH, N, d, causal, mode;
     float scale;        // alpha
     float scale_log2;   // alpha * log2(e)
+    float beta;         // stabilised-softmax shift factor (mode 1)
     int* status;        // device status word
     int num_sms;        // persistent grid: at most one CTA per SM
 };

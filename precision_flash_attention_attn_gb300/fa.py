@@ -34,6 +34,17 @@ _lib.fa_bwd.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, 
 _lib.fa_bwd_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P]
 _lib.fa_bwd_noalloc.restype = ctypes.c_int
 _lib.fa_tie_stats.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _P, _P, _P, _P]
+
+
+class StabParams(ctypes.Structure):
+    """fa_stab_params_t: beta (> 1) and eps (only 0 is supported)."""
+    _fields_ = [("beta", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+BETA_DEFAULT = 2.0
+_SP = ctypes.POINTER(StabParams)
+_lib.fa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P]
+_lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
 _lib.fa_profile_stop.argtypes = [_i, _P, _P]
@@ -42,7 +53,7 @@ _lib.fa_last_error.restype = ctypes.c_char_p
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
-            _lib.fa_profile_stop):
+            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex):
     _fn.restype = ctypes.c_int
 
 
@@ -101,6 +112,21 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, mode, stream=None, check=
     return _check("fa_fwd", rc) if check else rc
 
 
+def _params(beta, eps):
+    if beta is None and eps is None:
+        return None
+    return ctypes.pointer(StabParams(BETA_DEFAULT if beta is None else float(beta),
+                                     0.0 if eps is None else float(eps)))
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta=None, eps=None, stream=None,
+              check=True):
+    """fa_fwd with stabilised-softmax parameters (None: the library default)."""
+    rc = _lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(causal),
+                        float(scale), int(mode), _params(beta, eps), _stream(stream))
+    return _check("fa_fwd_ex", rc) if check else rc
+
+
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream=None, check=True):
     rc = _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
                      _ptr(dv), B, H, N, d, int(causal), float(scale), int(mode), _stream(stream))
@@ -125,6 +151,15 @@ def fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err,
     rc = _lib.fa_tie_stats(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, d, int(causal), float(scale),
                            int(mode), _ptr(tie_count), _ptr(pv_err), _ptr(p_one), _stream(stream))
     return _check("fa_tie_stats", rc) if check else rc
+
+
+def fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err, p_one=None,
+                    beta=None, eps=None, stream=None, check=True):
+    """fa_tie_stats with stabilised-softmax parameters (None: the library default)."""
+    rc = _lib.fa_tie_stats_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, d, int(causal), float(scale),
+                              int(mode), _params(beta, eps), _ptr(tie_count), _ptr(pv_err), _ptr(p_one),
+                              _stream(stream))
+    return _check("fa_tie_stats_ex", rc) if check else rc
 
 
 def fa_device_status(stream=None, reset=True) -> int:
@@ -156,15 +191,16 @@ def _shape(q):
     return B, H, N, d
 
 
-def attention_fwd(q, k, v, causal=True, scale=None, mode=0, stream=None):
-    """Returns (o, lse).  o is BF16, or FP32 in mode 2."""
+def attention_fwd(q, k, v, causal=True, scale=None, mode=0, stream=None, beta=None):
+    """Returns (o, lse).  o is BF16, or FP32 in mode 2.  beta: mode 1's shift
+    factor (None: the library default)."""
     import torch
     B, H, N, d = _shape(q)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty((B, H, N, d), device=q.device,
                     dtype=torch.float32 if mode == 2 else torch.bfloat16)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
-    fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, mode, stream)
+    fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta=beta, stream=stream)
     return o, lse
 
 
@@ -178,13 +214,13 @@ def attention_bwd(q, k, v, o, lse, dO, causal=True, scale=None, mode=0, stream=N
     return dq, dk, dv
 
 
-def tie_stats(q, k, v, o, causal=True, scale=None, mode=0, with_p_one=True, stream=None):
-    """Returns (tie_count, pv_err, p_one or None)."""
+def tie_stats(q, k, v, o, causal=True, scale=None, mode=0, with_p_one=True, stream=None, beta=None):
+    """Returns (tie_count, pv_err, p_one or None).  beta as for attention_fwd."""
     import torch
     B, H, N, d = _shape(q)
     scale = d ** -0.5 if scale is None else scale
     tc = torch.empty((B, H, N), device=q.device, dtype=torch.int32)
     pe = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     po = torch.empty((2, B, H, N), device=q.device, dtype=torch.int32) if with_p_one else None
-    fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, po, stream)
+    fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, po, beta=beta, stream=stream)
     return tc, pe, po

@@ -18,7 +18,8 @@ MISALIGNED = FAKE + 8
 def test_library_exports_every_declared_symbol():
     declared = fa.declared_symbols()
     assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
-                             "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc"}
+                             "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc",
+                             "fa_fwd_ex", "fa_tie_stats_ex"}
     lib = ctypes.CDLL(fa.library_path())
     for name in declared:
         assert hasattr(lib, name), name
@@ -98,3 +99,38 @@ def test_binding_raises_on_error():
     with pytest.raises(fa.FAError) as ei:
         fa.fa_fwd(0, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 1, 0.125, 0, stream=0)
     assert ei.value.status == 1
+
+
+def _fwd_ex(beta, eps, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, causal=1, scale=0.125,
+             mode=1, beta=beta, eps=eps, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_fwd_ex(**a)
+
+
+def _stats_ex(beta, eps, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, H=1, N=128, d=64, causal=1, scale=0.125, mode=1,
+             tie_count=FAKE, pv_err=FAKE, p_one=None, beta=beta, eps=eps, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_tie_stats_ex(**a)
+
+
+# "The modified safe softmax" requires beta > 1; only exact ties (eps = 0) are
+# supported, any other finite eps >= 0 is FA_ERR_UNSUPPORTED (2)
+BAD_PARAMS = [
+    (1.0, 0.0, 1), (0.5, 0.0, 1), (-2.0, 0.0, 1), (float("nan"), 0.0, 1), (float("inf"), 0.0, 1),
+    (2.0, -1e-3, 1), (2.0, float("nan"), 1), (2.0, float("inf"), 1), (2.0, 1e-3, 2), (8.0, 1.0, 2),
+]
+
+
+@pytest.mark.parametrize("beta,eps,code", BAD_PARAMS)
+def test_stab_params_rejected(beta, eps, code):
+    for mode in (0, 1, 2):  # checked in every mode, used only in mode 1
+        assert _fwd_ex(beta, eps, mode=mode) == code
+        assert _stats_ex(beta, eps, mode=mode) == code
+
+
+def test_argument_errors_precede_parameter_errors():
+    assert _fwd_ex(1.0, 0.0, q=0) == 1
+    assert _fwd_ex(2.0, 1e-3, d=96) == 2
+    assert _stats_ex(2.0, 1e-3, tie_count=0) == 1

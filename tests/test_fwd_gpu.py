@@ -21,9 +21,9 @@ def fa():
     return fa_mod
 
 
-def _run(fa, c, mode):
+def _run(fa, c, mode, beta=None):
     q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
-    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
+    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode, beta=beta)
     assert fa.fa_device_status() == 0
     return host_f64(o), host_f64(lse)
 
@@ -150,3 +150,20 @@ def test_stabilised_tie_decisions_agree_across_score_magnitudes(fa):
         assert np.array_equal(outs[(0, mode)], outs[(-42, mode)]), mode
         assert np.array_equal(outs[(0, mode)], outs[(14, mode)]), mode
     assert not np.array_equal(outs[(0, 0)], outs[(0, 1)])
+
+
+@pytest.mark.parametrize("beta", [4.0, 8.0])
+def test_stabilised_beta_parity(fa, beta):
+    # The shift factor is a run-time parameter ("The modified safe softmax":
+    # beta > 1, the authors use [2, 8]).  The exact output does not depend on
+    # it; the BF16 rounding of Pbar on tied rows does.
+    c = case("tiny")
+    o, lse = _run(fa, c, 1, beta=beta)
+    _check(c, o, lse, 1)
+    o2, _ = _run(fa, c, 1)
+    assert not np.array_equal(o, o2)
+    c = case("gpt2s")
+    o, lse = _run(fa, c, 1, beta=beta)
+    planted = np.flatnonzero(c.planted.reshape(-1))
+    rows = sample_rows(c.B * c.H, c.N, 256, seed=11, must=planted[::40])
+    _check(c, o, lse, 1, rows=rows)

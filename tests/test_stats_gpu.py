@@ -26,12 +26,12 @@ def _arrays(c):
     return [f32(getattr(c, n)).reshape(BH, c.N, c.d) for n in ("q", "k", "v")]
 
 
-def _stats(fa, c, mode, o=None):
+def _stats(fa, c, mode, o=None, beta=None):
     import torch
     q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
     if o is None:
-        o, _ = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
-    tc, pe, po = fa.tie_stats(q, k, v, o, c.causal, c.scale, mode)
+        o, _ = fa.attention_fwd(q, k, v, c.causal, c.scale, mode, beta=beta)
+    tc, pe, po = fa.tie_stats(q, k, v, o, c.causal, c.scale, mode, beta=beta)
     assert fa.fa_device_status() == 0
     torch.cuda.synchronize()
     return tc.cpu().numpy().reshape(-1), pe.cpu().numpy().reshape(-1).astype(np.float64), po.cpu().numpy().reshape(2, -1)
@@ -103,3 +103,35 @@ def test_stabilised_mode_has_no_unit_probability_on_tied_rows(fa):
     assert np.all(po1[0][keep] == 0) and np.all(po1[1][keep] == 0)
     assert np.all(po0[0][keep] >= tc0[keep])
     del smax, BH
+
+
+@pytest.mark.parametrize("beta", [4.0, 8.0])
+@pytest.mark.parametrize("name", ["tiny", "gpt2s"])
+def test_unit_probability_counts_match_emulation_beta(fa, name, beta):
+    # mode 1 with a run-time shift factor: the counts follow the emulation run
+    # with the same beta (the product beta * M is formed in FP32 on both sides)
+    c = case(name)
+    _, _, po = _stats(fa, c, 1, beta=beta)
+    qf, kf, vf = _arrays(c)
+    BH = c.B * c.H
+    rows = np.arange(BH * c.N) if name == "tiny" else \
+        np.random.default_rng(7).choice(BH * c.N, size=4096, replace=False)
+    em = orc.fwd_emul(qf, kf, vf, c.causal, c.scale, 1, beta=beta, block_n=128, rows=rows)
+    amb = em["p_amb"]
+    for idx, key in ((0, "p_one0"), (1, "p_one1")):
+        diff = np.abs(po[idx][rows] - em[key])
+        assert np.all(diff <= amb), (key, int(diff.max()))
+
+
+def test_stabilised_invariant_with_beta_8(fa):
+    # the invariant of the stabilised rule holds for any beta > 1: no Pbar = 1
+    # on planted-tie rows whose scaled max is not tiny
+    c = case("tiny")
+    tc0, _, _ = _stats(fa, c, 0)
+    _, _, po = _stats(fa, c, 1, beta=8.0)
+    qf, kf, _ = _arrays(c)
+    rows = np.flatnonzero(c.planted.reshape(-1) & (tc0 > 1))
+    s_max = np.array([max(qf[r // c.N, r % c.N] @ kf[r // c.N, j] for j in range((r % c.N) + 1)) for r in rows])
+    keep = rows[np.abs(c.scale * s_max) > 2.0 ** -8]
+    assert keep.size > 20
+    assert np.all(po[0][keep] == 0) and np.all(po[1][keep] == 0)
