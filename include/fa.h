@@ -185,13 +185,23 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o,
 
 /*
  * fa_tie_stats_ex -- fa_tie_stats with explicit stabilised-softmax parameters
- * (checked as by fa_fwd_ex).  The p_one counts of mode 1 follow beta; o must
- * come from fa_fwd_ex with the same parameters.
+ * (checked as by fa_fwd_ex), and optionally the error that the stored output
+ * brings into the backward's delta = rowsum(dO o O):
+ *   delta_err : nullable FP32 [B, H, N]; delta_err[r] = sum_c dO[r,c] *
+ *               (o[r,c] - O_ref[r,c]) with the same FP32 reference O_ref as
+ *               pv_err, i.e. delta_lp - delta_hp of section 3.4.4 ("Cause 2:
+ *               Biased Rounding Error Leads to Positive (delta_lp -
+ *               delta_hp)[T]"), O_ref standing in for the FP32 output O_hp;
+ *   dO        : BF16 [B, H, N, d], read only when delta_err is set (then
+ *               both must be 16-byte aligned device pointers).
+ * The p_one counts of mode 1 follow beta; o must come from fa_fwd_ex with the
+ * same parameters.
  */
 int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o,
                     int B, int H, int N, int d, int causal, float scale, int mode,
                     const fa_stab_params_t* params,
                     int32_t* tie_count, float* pv_err, int32_t* p_one,
+                    const void* dO, float* delta_err,
                     fa_stream_t stream);
 
 /*

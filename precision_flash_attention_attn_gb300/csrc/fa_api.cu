@@ -13,6 +13,7 @@
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "fa_stats.h"
 
 namespace {
 
@@ -383,14 +384,14 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int
                  int causal, float scale, int mode, int32_t* tie_count, float* pv_err, int32_t* p_one,
                  fa_stream_t stream) {
     return fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, nullptr, tie_count, pv_err, p_one,
-                           stream);
+                           nullptr, nullptr, stream);
 }
 
 int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
                     int causal, float scale, int mode, const fa_stab_params_t* params, int32_t* tie_count,
-                    float* pv_err, int32_t* p_one, fa_stream_t stream) {
+                    float* pv_err, int32_t* p_one, const void* dO, float* delta_err, fa_stream_t stream) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tie_count) ||
-        !aligned16(pv_err) || (p_one && !aligned16(p_one)))
+        !aligned16(pv_err) || (p_one && !aligned16(p_one)) || (delta_err && (!aligned16(delta_err) || !aligned16(dO))))
         return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
@@ -431,6 +432,8 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
     s.v = v;
     s.o = o;
     s.pv_err = pv_err;
+    s.dout = dO;
+    s.delta_err = delta_err;
     s.BH = BH;
     s.N = N;
     s.d = d;

@@ -51,17 +51,6 @@ struct BwdArgs {
     int num_sms;
 };
 
-struct StatsArgs {
-    const void* q;
-    const void* k;
-    const void* v;
-    const void* o;     // BF16 or FP32 (mode 2)
-    float* pv_err;     // [BH, N]
-    int BH, N, d, causal, mode;
-    float scale;
-    int* status;
-};
-
 // Record the CUDA error behind a failing step (read back by fa_last_error).
 void set_error(const char* step, cudaError_t e);
 void set_error_msg(const char* step, const char* msg);
@@ -88,6 +77,5 @@ inline cudaError_t smem_limit_once(Kernel kern, int bytes, unsigned* done) {
 
 cudaError_t launch_fwd(const FwdArgs& a, bool stats, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_pv_err(const StatsArgs& a, cudaStream_t stream);
 
 }  // namespace fa

@@ -4,7 +4,10 @@
 // with the exact row maximum and compensated (Kahan) sums, independently of
 // the tensor-core forward ("Why Low-Precision Transformer Training Fails: An
 // Analysis on Flash Attention", section 3.4.4, "Isolating the error to PV":
-// the low-precision result minus the FP32 result).  Diagnostic only.
+// the low-precision result minus the FP32 result).  Optionally also the error
+// of the backward's delta = rowsum(dO o O) that the stored output causes,
+//   delta_err[r] = sum_c dO[r,c] * (o[r,c] - O_ref[r,c])  (= delta_lp - delta_hp,
+// section 3.4.4 "Cause 2", with O_ref standing in for O_hp).  Diagnostic only.
 //
 // One CTA = 128 query rows of one (batch, head), one thread per row.  Keys are
 // staged 32 at a time in shared memory as FP32.  Pass 1 finds the row max;
@@ -13,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "fa_stats.h"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -74,6 +78,7 @@ __global__ void __launch_bounds__(128) pv_err_kernel(const StatsArgs a) {
 
     Kahan l;
     Kahan err;
+    Kahan derr;
     for (int c0 = 0; c0 < D; c0 += KC) {
         Kahan acc[KC];
         for (int j0 = 0; j0 < kend; j0 += KC) {
@@ -99,11 +104,16 @@ __global__ void __launch_bounds__(128) pv_err_kernel(const StatsArgs a) {
             for (int c = 0; c < KC; ++c) {
                 const size_t idx = head + static_cast<size_t>(i) * D + c0 + c;
                 const float oc = (a.mode == 2) ? static_cast<const float*>(a.o)[idx] : bf16_at(a.o, idx);
-                err.add(oc - acc[c].s * inv);
+                const float e = oc - acc[c].s * inv;
+                err.add(e);
+                if (a.delta_err) derr.add(bf16_at(a.dout, idx) * e);
             }
         }
     }
-    if (valid) a.pv_err[static_cast<size_t>(bh) * a.N + i] = err.s;
+    if (valid) {
+        a.pv_err[static_cast<size_t>(bh) * a.N + i] = err.s;
+        if (a.delta_err) a.delta_err[static_cast<size_t>(bh) * a.N + i] = derr.s;
+    }
 }
 
 }  // namespace

@@ -44,7 +44,7 @@ class StabParams(ctypes.Structure):
 BETA_DEFAULT = 2.0
 _SP = ctypes.POINTER(StabParams)
 _lib.fa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P]
-_lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P]
+_lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
 _lib.fa_profile_stop.argtypes = [_i, _P, _P]
@@ -154,11 +154,12 @@ def fa_tie_stats(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err,
 
 
 def fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_err, p_one=None,
-                    beta=None, eps=None, stream=None, check=True):
-    """fa_tie_stats with stabilised-softmax parameters (None: the library default)."""
+                    dO=None, delta_err=None, beta=None, eps=None, stream=None, check=True):
+    """fa_tie_stats with stabilised-softmax parameters (None: the library
+    default) and, with dO and delta_err, the per-row delta error."""
     rc = _lib.fa_tie_stats_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, N, d, int(causal), float(scale),
                               int(mode), _params(beta, eps), _ptr(tie_count), _ptr(pv_err), _ptr(p_one),
-                              _stream(stream))
+                              _ptr(dO), _ptr(delta_err), _stream(stream))
     return _check("fa_tie_stats_ex", rc) if check else rc
 
 
@@ -224,3 +225,17 @@ def tie_stats(q, k, v, o, causal=True, scale=None, mode=0, with_p_one=True, stre
     po = torch.empty((2, B, H, N), device=q.device, dtype=torch.int32) if with_p_one else None
     fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, po, beta=beta, stream=stream)
     return tc, pe, po
+
+
+def delta_error(q, k, v, o, dO, causal=True, scale=None, mode=0, stream=None, beta=None):
+    """Per-row delta_lp - delta_hp = sum_c dO (o - O_ref) of the stored output
+    o (FP32 [B, H, N]), from fa_tie_stats_ex."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    tc = torch.empty((B, H, N), device=q.device, dtype=torch.int32)
+    pe = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    de = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, None, dO=dO, delta_err=de, beta=beta,
+                    stream=stream)
+    return de

@@ -134,3 +134,10 @@ def test_argument_errors_precede_parameter_errors():
     assert _fwd_ex(1.0, 0.0, q=0) == 1
     assert _fwd_ex(2.0, 1e-3, d=96) == 2
     assert _stats_ex(2.0, 1e-3, tie_count=0) == 1
+
+
+def test_delta_err_needs_dO():
+    # delta_err is nullable; when set, dO must be a 16-byte aligned pointer too
+    assert _stats_ex(2.0, 0.0, delta_err=FAKE, dO=None) == 1
+    assert _stats_ex(2.0, 0.0, delta_err=FAKE, dO=MISALIGNED) == 1
+    assert _stats_ex(2.0, 0.0, delta_err=MISALIGNED, dO=FAKE) == 1

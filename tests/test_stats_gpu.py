@@ -135,3 +135,42 @@ def test_stabilised_invariant_with_beta_8(fa):
     keep = rows[np.abs(c.scale * s_max) > 2.0 ** -8]
     assert keep.size > 20
     assert np.all(po[0][keep] == 0) and np.all(po[1][keep] == 0)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_delta_err_matches_oracle(fa, mode):
+    # delta_lp - delta_hp = sum_c dO (O - O_hp) ("Cause 2: Biased Rounding Error
+    # Leads to Positive (delta_lp - delta_hp)[T]"), for an output O produced by
+    # the oracle's emulation, against the oracle's exact output as O_hp
+    import torch
+    c = case("tiny")
+    qf, kf, vf = _arrays(c)
+    ex = orc.fwd(qf, kf, vf, c.causal, c.scale, 0)
+    em = orc.fwd_emul(qf, kf, vf, c.causal, c.scale, mode, block_n=128)
+    o_in = em["o"].reshape(c.q.shape)
+    if mode == 2:
+        o_dev = torch.from_numpy(o_in.astype(np.float32)).cuda()
+    else:
+        o_dev = dev_bf16(bf16_bits(o_in.astype(np.float32)))
+    q, k, v, g = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    de = fa.delta_error(q, k, v, o_dev, g, c.causal, c.scale, mode)
+    assert fa.fa_device_status() == 0
+    gf = f32(c.do).reshape(-1, c.d).astype(np.float64)
+    want = (gf * (o_in.reshape(-1, c.d) - ex["o"].reshape(-1, c.d))).sum(1)
+    np.testing.assert_allclose(de.cpu().numpy().reshape(-1), want, rtol=0, atol=2e-4 * max(1.0, np.abs(gf).max()))
+
+
+def test_delta_err_with_unit_gradient_is_pv_err(fa):
+    # with dO = 1 the weighted sum is the plain one, term for term
+    import torch
+    c = case("tiny")
+    q, k, v = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v"))
+    o, _ = fa.attention_fwd(q, k, v, c.causal, c.scale, 0)
+    ones = torch.ones_like(q)
+    B, H, N, d = q.shape
+    tc = torch.empty((B, H, N), device="cuda", dtype=torch.int32)
+    pe = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+    de = torch.empty_like(pe)
+    fa.fa_tie_stats_ex(q, k, v, o, B, H, N, d, c.causal, c.scale, 0, tc, pe, None, dO=ones, delta_err=de)
+    assert fa.fa_device_status() == 0
+    assert torch.equal(pe, de)
