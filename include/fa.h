@@ -132,6 +132,31 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            fa_stream_t stream);
 
 /*
+ * fa_bwd_ex -- fa_bwd with a choice of the output that delta =
+ * rowsum(dO o O) is formed from (section 3.4.2, "Isolation Experiments:
+ * Narrowing Down the Failure Source"):
+ *   FA_DELTA_STORED_O          the caller's o, as fa_bwd does (o in `mode`'s
+ *                              dtype);
+ *   FA_DELTA_RECOMPUTED_O_FP32 O recomputed inside the backward as P V in FP32:
+ *                              the forward runs in FA_MODE_FP32_OUT into a
+ *                              stream-ordered workspace of B*H*N*(d+1)*4 bytes
+ *                              (cudaMallocAsync on `stream`, on top of
+ *                              fa_bwd's), and delta is formed from it; o is
+ *                              not read and may be NULL.
+ * P is recomputed from the caller's lse either way, so only delta's source
+ * changes.  Other arguments and errors as fa_bwd; FA_ERR_INVALID_ARG for an
+ * unknown delta_source.
+ */
+typedef enum {
+    FA_DELTA_STORED_O = 0,
+    FA_DELTA_RECOMPUTED_O_FP32 = 1
+} fa_delta_source_t;
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dO, void* dq, void* dk, void* dv,
+              int B, int H, int N, int d, int causal, float scale, int mode,
+              int delta_source, fa_stream_t stream);
+
+/*
  * fa_bwd_noalloc -- the same backward as fa_bwd, for callers that must not
  * allocate device memory: code that runs after a framework's caching
  * allocator has reserved (nearly) all of the GPU's memory, so a driver

@@ -281,6 +281,42 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// Backward with delta formed from O recomputed in FP32 (the forward in mode 2
+// into a workspace), or from the caller's o.
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+              void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
+              int delta_source, fa_stream_t stream) {
+    if (delta_source == FA_DELTA_STORED_O)
+        return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream);
+    if (delta_source != FA_DELTA_RECOMPUTED_O_FP32) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const size_t o_bytes = static_cast<size_t>(B) * H * N * d * sizeof(float);  // a multiple of 256
+    const size_t lse_bytes = static_cast<size_t>(B) * H * N * sizeof(float);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
+    if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    cudaError_t ae = cudaMallocAsync(&ws, o_bytes + lse_bytes, st);
+    if (ae != cudaSuccess || !ws) {
+        fa::set_error("cudaMallocAsync(recomputed O)", ae);
+        cudaGetLastError();
+        return FA_ERR_ALLOC;
+    }
+    float* o32 = static_cast<float*>(ws);
+    float* lse32 = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+    rc = fa_fwd_ex(q, k, v, o32, lse32, B, H, N, d, causal, scale, FA_MODE_FP32_OUT, nullptr, stream);
+    if (rc == FA_OK) rc = fa_bwd(q, k, v, o32, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, FA_MODE_FP32_OUT, stream);
+    const cudaError_t fe = cudaFreeAsync(ws, st);
+    if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(recomputed O)", fe);
+    return rc;
+}
+
 // Allocation-free backward: the workspace is a file-scope device array.
 // ---------------------------------------------------------------------------
 namespace {

@@ -44,6 +44,9 @@ class StabParams(ctypes.Structure):
 BETA_DEFAULT = 2.0
 _SP = ctypes.POINTER(StabParams)
 _lib.fa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P]
+_lib.fa_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _i, _P]
+DELTA_STORED_O = 0            # delta from the caller's o (fa_bwd)
+DELTA_RECOMPUTED_O_FP32 = 1   # delta from O recomputed as P V in FP32 inside the backward
 _lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
@@ -53,7 +56,7 @@ _lib.fa_last_error.restype = ctypes.c_char_p
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
-            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex):
+            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex):
     _fn.restype = ctypes.c_int
 
 
@@ -133,6 +136,15 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, str
     return _check("fa_bwd", rc) if check else rc
 
 
+def fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, delta_source=DELTA_STORED_O,
+              stream=None, check=True):
+    """fa_bwd with a choice of the output delta is formed from (o may be None
+    with DELTA_RECOMPUTED_O_FP32)."""
+    rc = _lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, H, N, d, int(causal), float(scale), int(mode), int(delta_source), _stream(stream))
+    return _check("fa_bwd_ex", rc) if check else rc
+
+
 def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream=None,
                    check=True):
     """fa_bwd with its workspace in the library's static scratch array
@@ -205,13 +217,14 @@ def attention_fwd(q, k, v, causal=True, scale=None, mode=0, stream=None, beta=No
     return o, lse
 
 
-def attention_bwd(q, k, v, o, lse, dO, causal=True, scale=None, mode=0, stream=None):
+def attention_bwd(q, k, v, o, lse, dO, causal=True, scale=None, mode=0, stream=None,
+                  delta_source=DELTA_STORED_O):
     """Returns (dq, dk, dv), BF16."""
     import torch
     B, H, N, d = _shape(q)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream)
+    fa_bwd_ex(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, delta_source, stream)
     return dq, dk, dv
 
 

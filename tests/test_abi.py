@@ -19,7 +19,7 @@ def test_library_exports_every_declared_symbol():
     declared = fa.declared_symbols()
     assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
                              "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc",
-                             "fa_fwd_ex", "fa_tie_stats_ex"}
+                             "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex"}
     lib = ctypes.CDLL(fa.library_path())
     for name in declared:
         assert hasattr(lib, name), name
@@ -141,3 +141,25 @@ def test_delta_err_needs_dO():
     assert _stats_ex(2.0, 0.0, delta_err=FAKE, dO=None) == 1
     assert _stats_ex(2.0, 0.0, delta_err=FAKE, dO=MISALIGNED) == 1
     assert _stats_ex(2.0, 0.0, delta_err=MISALIGNED, dO=FAKE) == 1
+
+
+def _bwd_ex(source, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=1,
+             N=128, d=64, causal=1, scale=0.125, mode=0, delta_source=source, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_bwd_ex(**a)
+
+
+@pytest.mark.parametrize("source", [2, -1, 100])
+def test_bwd_ex_unknown_delta_source(source):
+    assert _bwd_ex(source) == 1
+
+
+@pytest.mark.parametrize("source", [0, 1])
+@pytest.mark.parametrize("kw", [dict(q=0), dict(dO=0), dict(dq=MISALIGNED), dict(lse=0), dict(N=0), dict(mode=3)])
+def test_bwd_ex_invalid_arguments(source, kw):
+    assert _bwd_ex(source, **kw) == 1
+
+
+def test_bwd_ex_stored_o_still_needs_o():
+    assert _bwd_ex(0, o=0) == 1

@@ -119,3 +119,26 @@ def test_alloc_failure_is_reported(fa, monkeypatch):
     dq, dk, dv = (q.clone() for _ in range(3))
     rc = fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, c.B, c.H, c.N, c.d, True, c.scale, 0, check=False)
     assert rc == 3
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_delta_from_recomputed_fp32_output(fa, mode):
+    # The isolation experiment of section 3.4.2: delta from O recomputed as P V
+    # in FP32 inside the backward.  Gradients stay within the oracle's bound,
+    # and dK/dV are bit-identical to a backward fed the FP32-output forward's O
+    # with the same LSE (the forward is deterministic; only delta's source
+    # differs from the stored-O backward).
+    import torch
+    c = case("tiny")
+    q, k, v, do = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
+    got = fa.attention_bwd(q, k, v, None, lse, do, c.causal, c.scale, mode,
+                           delta_source=fa.DELTA_RECOMPUTED_O_FP32)
+    assert fa.fa_device_status() == 0
+    _check_full(c, mode, [host_f64(t) for t in got])
+    o32, _ = fa.attention_fwd(q, k, v, c.causal, c.scale, 2)
+    ref = fa.attention_bwd(q, k, v, o32, lse, do, c.causal, c.scale, 2)
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    assert (got[0].float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
+    stored = fa.attention_bwd(q, k, v, o, lse, do, c.causal, c.scale, mode)
+    assert not torch.equal(stored[1], got[1])  # delta's source matters
