@@ -1,0 +1,92 @@
+"""Sweep of the stabilised softmax's shift factor beta on a tie-heavy workload.
+
+"The modified safe softmax" (section 3.4.5 of "Why Low-Precision Transformer
+Training Fails: An Analysis on Flash Attention") requires beta > 1 and names
+[2, 8] as the authors' range, and the page notes that no sweep over beta is
+reported.  For the baseline and for each beta this runs the forward
+(fa_fwd_ex) and the tie statistics (fa_tie_stats_ex) on one workload, and
+reports over the rows with a planted tie whose exact tie count is > 1:
+
+  * p_one0_rows:  fraction of those rows that fed at least one Pbar = 1 to PV;
+  * p_one1_mean:  mean number of keys whose final weight is exactly 1;
+  * pv_err:       mean and standard error of sum_c (O - O_ref);
+  * delta_err:    mean and standard error of sum_c dO (O - O_ref), the error
+                  of the backward's delta (section 3.4.4, "Cause 2");
+  * nonfinite_rows: rows whose output is not finite (a large beta underflows
+                  every Pbar of a row with a large repeated maximum), which the
+                  means leave out.
+
+Usage: python -m precision_flash_attention_attn_gb300.beta_sweep [--betas 2,4,8] [--workload ties]
+Prints one JSON line per setting.  Needs a GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+
+import numpy as np
+
+
+def _mean_se(x: np.ndarray):
+    if x.size == 0:
+        return None, None
+    se = float(x.std(ddof=1) / math.sqrt(x.size)) if x.size > 1 else None
+    return float(x.mean()), se
+
+
+def main(argv=None) -> int:
+    import torch
+
+    from . import fa
+    from .inputs import make_case
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--betas", default="2,4,8")
+    ap.add_argument("--workload", default="ties")
+    args = ap.parse_args(argv)
+    betas = [float(b) for b in args.betas.split(",") if b.strip()]
+
+    c = make_case(args.workload)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    q, k, v, do = (to_dev(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    B, H, N, d = c.B, c.H, c.N, c.d
+
+    def run(mode, beta):
+        o, _ = fa.attention_fwd(q, k, v, c.causal, c.scale, mode, beta=beta)
+        tc = torch.empty((B, H, N), device="cuda", dtype=torch.int32)
+        pe = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+        de = torch.empty_like(pe)
+        po = torch.empty((2, B, H, N), device="cuda", dtype=torch.int32)
+        fa.fa_tie_stats_ex(q, k, v, o, B, H, N, d, c.causal, c.scale, mode, tc, pe, po, dO=do, delta_err=de,
+                           beta=beta)
+        finite = torch.isfinite(o.float()).all(-1)
+        if fa.fa_device_status() != 0:
+            raise RuntimeError("kernel timeout")
+        return (tc.cpu().numpy().reshape(-1), pe.cpu().numpy().reshape(-1).astype(np.float64),
+                po.cpu().numpy().reshape(2, -1), de.cpu().numpy().reshape(-1).astype(np.float64),
+                finite.cpu().numpy().reshape(-1))
+
+    tc0 = run(0, None)[0]
+    rows = np.flatnonzero(c.planted.reshape(-1) & (tc0 > 1))
+    settings = [("baseline", 0, None)] + [(f"stabilised beta={b:g}", 1, b) for b in betas]
+    for name, mode, beta in settings:
+        _, pe, po, de, finite = run(mode, beta)
+        ok = rows[finite[rows]]
+        pv_m, pv_se = _mean_se(pe[ok])
+        de_m, de_se = _mean_se(de[ok])
+        print(json.dumps({
+            "workload": args.workload, "setting": name, "tied_rows": int(rows.size),
+            "p_one0_rows": float((po[0][rows] > 0).mean()) if rows.size else None,
+            "p_one1_mean": float(po[1][rows].mean()) if rows.size else None,
+            "pv_err": {"mean": pv_m, "se": pv_se}, "delta_err": {"mean": de_m, "se": de_se},
+            "nonfinite_rows": int((~finite).sum()), "nonfinite_tied_rows": int(rows.size - ok.size),
+        }), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

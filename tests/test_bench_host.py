@@ -68,3 +68,12 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_beta_sweep_mean_and_standard_error():
+    import numpy as np
+    from precision_flash_attention_attn_gb300.beta_sweep import _mean_se
+    m, se = _mean_se(np.array([1.0, 2.0, 3.0, 6.0]))
+    assert m == 3.0 and abs(se - np.std([1.0, 2.0, 3.0, 6.0], ddof=1) / 2.0) < 1e-15
+    assert _mean_se(np.array([])) == (None, None)
+    assert _mean_se(np.array([4.0])) == (4.0, None)

@@ -174,3 +174,18 @@ def test_delta_err_with_unit_gradient_is_pv_err(fa):
     fa.fa_tie_stats_ex(q, k, v, o, B, H, N, d, c.causal, c.scale, 0, tc, pe, None, dO=ones, delta_err=de)
     assert fa.fa_device_status() == 0
     assert torch.equal(pe, de)
+
+
+def test_beta_sweep_runs_on_tiny(fa, capsys):
+    # the sweep module end to end: one line per setting; the baseline feeds
+    # Pbar = 1 on every tied row, the stabilised settings leave fewer keys
+    # with a final weight of exactly 1, and nothing underflows at this scale
+    import json
+    from precision_flash_attention_attn_gb300 import beta_sweep
+    assert beta_sweep.main(["--workload", "tiny", "--betas", "2,8"]) == 0
+    lines = [json.loads(ln) for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert [ln["setting"] for ln in lines] == ["baseline", "stabilised beta=2", "stabilised beta=8"]
+    assert lines[0]["tied_rows"] > 20 and lines[0]["p_one0_rows"] == 1.0
+    for ln in lines[1:]:
+        assert ln["p_one1_mean"] < lines[0]["p_one1_mean"]
+        assert ln["nonfinite_rows"] == 0
