@@ -7,9 +7,11 @@ scale 1/8; seeded synthetic BF16 inputs with 5% planted tied-max rows).
 Throughput counts 12*d algorithmic FLOP per visible (query, key) pair per mode
 (4d forward: QK^T and PV; 8d backward: dP, dV, dK, dQ; the backward's
 recomputation of S is not counted).  The timed steps run as one launch of a
-CUDA graph captured from the fa_fwd / fa_bwd_noalloc calls (the L2 flush and
-the step and mode events are graph nodes too); the end-to-end figure runs
-fa_fwd / fa_bwd call by call with the host copies.
+CUDA graph captured from the fa_fwd / fa_bwd_noalloc calls (fa_bwd where the
+no-alloc scratch is too small; the L2 flush and the step and mode events are
+graph nodes too); the end-to-end figure runs fa_fwd / fa_bwd call by call
+with the host copies.  --workload selects another input set for profiling
+(gpt2m, long, ties); the headline is gpt2s.
 
 Prints one JSON line.  ``--impl reference`` times the CPU FP64 oracle instead
 (the only reference implementation of this method available), on a bounded
@@ -60,7 +62,16 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="gpt2s", choices=["gpt2s", "gpt2m", "long", "ties"],
+                    help="input set of the GPU arm (the headline is gpt2s; the others are for profiling)")
     return ap.parse_args()
+
+
+def workload_name(case) -> str:
+    if case.spec.name == "gpt2s":
+        return WORKLOAD
+    kind = "causal" if case.causal else "full"
+    return f"{case.spec.name} attention: B={case.B} H={case.H} N={case.N} d={case.d} {kind}, fwd+bwd x 3 modes"
 
 
 def dist_env():
@@ -101,15 +112,15 @@ def sources_sha(kernel):
     return h.hexdigest()
 
 
-def recorded_traffic(kernel):
+def recorded_traffic(kernel, workload="gpt2s"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current sources of that kernel."""
+    on the current sources of that kernel and on the same workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f).get(kernel)
-    if not rec or rec.get("source_sha256") != sources_sha(kernel):
+    if not rec or rec.get("source_sha256") != sources_sha(kernel) or rec.get("workload") != workload:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -260,7 +271,7 @@ def run_ours(args):
     from precision_flash_attention_attn_gb300 import fa
     from precision_flash_attention_attn_gb300.inputs import make_case
 
-    case = make_case("gpt2s")
+    case = make_case(args.workload)
     B, H, N, d, causal, scale = case.B, case.H, case.N, case.d, case.causal, case.scale
     pairs = visible_pairs(B, H, N, causal)
     flop_mode = 12 * d * pairs
@@ -284,10 +295,14 @@ def run_ours(args):
         fa.fa_fwd(qq, kk, vv, b["o"], b["lse"], B, H, N, d, causal, scale, m, st)
         bwd(qq, kk, vv, b["o"], b["lse"], gg, b["dq"], b["dk"], b["dv"], B, H, N, d, causal, scale, m, st)
 
+    # the allocation-free backward where its static scratch holds the workspace
+    ws_bytes = B * H * N * d * 4 + 2 * B * H * ((N + 127) // 128 * 128) * 4
+    bwd_timed = fa.fa_bwd_noalloc if ws_bytes <= fa.NOALLOC_SCRATCH_BYTES else fa.fa_bwd
+    bwd_name = "fa_bwd_noalloc" if bwd_timed is fa.fa_bwd_noalloc else "fa_bwd"
     for _ in range(args.warmup):
         flush.zero_()
         for _, m in MODES:
-            one_mode(m, bwd=fa.fa_bwd_noalloc)
+            one_mode(m, bwd=bwd_timed)
     torch.cuda.synchronize()
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel timeout during warm-up")
@@ -312,7 +327,7 @@ def run_ours(args):
                     flush.zero_()
                     evs[s][0].record(cap)
                     for i, (_, m) in enumerate(MODES):
-                        one_mode(m, st=cap, bwd=fa.fa_bwd_noalloc)
+                        one_mode(m, st=cap, bwd=bwd_timed)
                         evs[s][i + 1].record(cap)
         except Exception:
             if kernel_events:
@@ -321,7 +336,7 @@ def run_ours(args):
         return g, evs
 
     graph = graph_k = ev_k = None
-    timing = (f"one CUDA graph launch of the {args.steps} steps (captured fa_fwd + fa_bwd_noalloc calls); "
+    timing = (f"one CUDA graph launch of the {args.steps} steps (captured fa_fwd + {bwd_name} calls); "
               "per-kernel durations from a second launch with an event pair per kernel")
     try:
         graph, ev = capture(False)
@@ -363,7 +378,7 @@ def run_ours(args):
             e = ev[s]
             e[0].record(stream)
             for i, (_, m) in enumerate(MODES):
-                one_mode(m, bwd=fa.fa_bwd_noalloc)
+                one_mode(m, bwd=bwd_timed)
                 e[i + 1].record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -432,7 +447,7 @@ def run_ours(args):
         achieved = flop_launch / (avg_ms * 1e-3) / 1e12
         peak = float(peaks["bf16_tflops"])
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(dom),
+                "frac": achieved / peak, "traffic": recorded_traffic(dom, args.workload),
                 "flop_per_launch": flop_launch, "avg_launch_ms": avg_ms,
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
     kernel_share = {kname: {"launches": v[0], "total_ms": v[1], "share": v[1] / sum(x[1] for x in timed.values())}
@@ -443,7 +458,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
+        "config": {"workload": workload_name(case), "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
                    "modes": [n for n, _ in MODES], "planted_tie_rows": 0.05,
                    "flop_per_step": flop_step, "flop_convention": "12*d per visible pair per mode",
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",

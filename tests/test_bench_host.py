@@ -77,3 +77,13 @@ def test_beta_sweep_mean_and_standard_error():
     assert m == 3.0 and abs(se - np.std([1.0, 2.0, 3.0, 6.0], ddof=1) / 2.0) < 1e-15
     assert _mean_se(np.array([])) == (None, None)
     assert _mean_se(np.array([4.0])) == (4.0, None)
+
+
+def test_recorded_traffic_only_for_its_workload():
+    # the committed DRAM figures belong to one workload; another workload's
+    # roofline must not borrow them
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.recorded_traffic("bwd_main", "long") is None
+    assert bench.recorded_traffic("fwd", "ties") is None
+    assert bench.recorded_traffic("no_such_kernel") is None
