@@ -21,7 +21,10 @@
  *   - section 3.4.4, "Concrete bit-level example": BF16 round-to-nearest-even.
  *
  * Readings of the pages used here:
- *   - eps = 0: a tie is exact equality of raw scores q.k;
+ *   - eps = 0 (the default): a tie is exact equality of raw scores q.k; with
+ *     eps > 0 (the exact forward only) keys whose scaled score lies within eps
+ *     of the scaled row maximum, alpha*(rm - s) <= eps, count toward rs, over
+ *     the whole row as the section's untiled rule states;
  *   - scores are scaled by alpha > 0 before the exponential; the shift rule is
  *     applied to the scaled scores (the sign tests do not depend on alpha > 0);
  *   - causal: key j is visible to query i iff j <= i;
@@ -78,7 +81,7 @@ double oracle_row_shift(double rmz, long rs, int mode, double beta) {
 
 /* Forward for one row: O row, LSE, tie count; s is scratch of length N. */
 static void fwd_row(const float* q, const float* k, const float* v, int N, int d, int i,
-                    int causal, double alpha, int mode, double beta, double* s,
+                    int causal, double alpha, int mode, double beta, double eps, double* s,
                     double* o, double* lse, int32_t* ties) {
     int nv = n_visible(i, N, causal);
     double rm = -INFINITY;
@@ -87,7 +90,7 @@ static void fwd_row(const float* q, const float* k, const float* v, int N, int d
         if (s[j] > rm) rm = s[j];
     }
     long rs = 0;
-    for (int j = 0; j < nv; ++j) rs += (s[j] == rm);
+    for (int j = 0; j < nv; ++j) rs += (eps == 0.0) ? (s[j] == rm) : (alpha * (rm - s[j]) <= eps);
     double m = row_shift(alpha * rm, rs, mode, beta);
     double l = 0.0;
     for (int c = 0; c < d; ++c) o[c] = 0.0;
@@ -107,7 +110,7 @@ static void fwd_row(const float* q, const float* k, const float* v, int N, int d
  * delta[r] = sum_c dO[r,c] * O[r,c] (the backward's rowsum(dO o O)). */
 int oracle_fwd(const float* q, const float* k, const float* v, const float* dout,
                int64_t BH, int N, int d, int causal, double alpha, int mode, double beta,
-               const int64_t* rows, int64_t nrows,
+               double eps, const int64_t* rows, int64_t nrows,
                double* o, double* lse, int32_t* ties, double* delta) {
     if (!rows) nrows = BH * (int64_t)N;
     int err = 0;
@@ -125,7 +128,7 @@ int oracle_fwd(const float* q, const float* k, const float* v, const float* dout
             int64_t bh = flat / N;
             int i = (int)(flat % N);
             const size_t off = (size_t)bh * N * d;
-            fwd_row(q + off, k + off, v + off, N, d, i, causal, alpha, mode, beta, s,
+            fwd_row(q + off, k + off, v + off, N, d, i, causal, alpha, mode, beta, eps, s,
                     o + (size_t)r * d, lse ? lse + r : NULL, ties ? ties + r : NULL);
             if (dout && delta) {
                 const float* g = dout + off + (size_t)i * d;

@@ -45,7 +45,7 @@ def lib():
         L = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        L.oracle_fwd.argtypes = [P, P, P, P, i64, i32, i32, i32, f64, i32, f64, P, i64, P, P, P, P]
+        L.oracle_fwd.argtypes = [P, P, P, P, i64, i32, i32, i32, f64, i32, f64, f64, P, i64, P, P, P, P]
         L.oracle_bwd_dq.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, f64, P, i64, P]
         L.oracle_bwd_dkdv.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, f64, P, i64, P, P]
         L.oracle_bf16_round.argtypes = [P, P, i64]
@@ -95,10 +95,13 @@ def bf16_round(x) -> np.ndarray:
     return y
 
 
-def fwd(q, k, v, causal, scale, mode=0, beta=BETA, rows=None, dout=None):
+def fwd(q, k, v, causal, scale, mode=0, beta=BETA, rows=None, dout=None, eps=0.0):
     """Exact attention forward.  Returns dict(o, lse, ties[, delta]); with
     rows=None every row of every head in [BH, N] order, else the listed flat
-    rows (bh*N + i) in that order."""
+    rows (bh*N + i) in that order.  ties is the row's rs of section 3.4.5:
+    keys at the maximum (eps = 0) or within eps of it in scaled units."""
+    if not eps >= 0.0:
+        raise ValueError("eps must be >= 0")
     q, k, v = _f32(q), _f32(k), _f32(v)
     BH, N, d = q.shape
     r, nr = _rows(rows)
@@ -109,7 +112,7 @@ def fwd(q, k, v, causal, scale, mode=0, beta=BETA, rows=None, dout=None):
     delta = np.empty(n, np.float64) if dout is not None else None
     g = _f32(dout) if dout is not None else None
     rc = lib().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), BH, N, d, int(causal), float(scale),
-                          int(mode), float(beta), _ptr(r), nr, _ptr(o), _ptr(lse), _ptr(ties),
+                          int(mode), float(beta), float(eps), _ptr(r), nr, _ptr(o), _ptr(lse), _ptr(ties),
                           _ptr(delta))
     if rc:
         raise MemoryError("oracle_fwd failed")

@@ -347,3 +347,52 @@ def test_per_addition_rounding_hand_worked():
     assert em["o_peradd"][0, 2, 0] == -5.6875 / 3
     assert ex["o"][0, 2, 0] == pytest.approx(-5.703125 / 3, rel=1e-15)
     assert em["p_one0"][0, 2] == 3
+
+
+# Near-tie tolerance eps > 0 (section 3.4.5, "rs = rowsum(rm - S <= eps)"): one
+# query e_0 against keys whose first component is a chosen BF16-exact value,
+# so the raw score of key j is exactly A[j] and the distances to the maximum
+# 1.5 are known by construction: 0 (twice), 2^-7 (twice), 2^-4, 0.25, 1, 2.5.
+_EPS_A = [1.5, 1.4921875, 1.4375, 1.5, 0.5, 1.4921875, -1.0, 1.25]
+
+
+def _eps_inputs():
+    N, d = len(_EPS_A), 4
+    q = np.zeros((1, N, d), np.float32)
+    q[0, :, 0] = 1.0
+    k = np.zeros((1, N, d), np.float32)
+    k[0, :, 0] = _EPS_A
+    v = bf16_bits_to_f32(bf16_bits(np.random.default_rng(5).standard_normal((1, N, d)).astype(np.float32)))
+    return q, k, v
+
+
+@pytest.mark.parametrize("scale,eps,count", [
+    (1.0, 0.0, 2), (1.0, 0.005, 2), (1.0, 0.0078125, 4), (1.0, 0.01, 4), (1.0, 0.0625, 5),
+    (1.0, 0.3, 6), (1.0, 3.0, 8),
+    (0.5, 0.0038, 2), (0.5, 0.004, 4), (0.5, 0.03, 4), (0.5, 0.032, 5), (0.5, 0.12, 5), (0.5, 0.13, 6),
+])
+def test_near_tie_counts_by_construction(scale, eps, count):
+    q, k, v = _eps_inputs()
+    f = orc.fwd(q, k, v, 0, scale, 1, eps=eps)
+    assert np.all(f["ties"] == count)
+
+
+def test_near_tie_counts_causal_prefixes():
+    # causal row i sees keys 0..i only: count the constructed distances by hand
+    q, k, v = _eps_inputs()
+    f = orc.fwd(q, k, v, 1, 1.0, 1, eps=0.01)
+    # prefixes: [1.5] -> 1; +1.4921875 -> 2; +1.4375 (2^-4 away) -> 2; +1.5 -> 3
+    # (two maxima, one near); +0.5 -> 3; +1.4921875 -> 4; +(-1) -> 4; +1.25 -> 4
+    assert f["ties"].reshape(-1).tolist() == [1, 2, 2, 3, 3, 4, 4, 4]
+
+
+def test_near_tie_shift_keeps_the_exact_output():
+    # a shift decided by near ties is still a shift: O and LSE do not move
+    q, k, v = _eps_inputs()
+    base = orc.fwd(q, k, v, 0, 1.0, 0)
+    for eps in (0.0, 0.01, 3.0):
+        f = orc.fwd(q, k, v, 0, 1.0, 1, eps=eps)
+        np.testing.assert_allclose(f["o"], base["o"], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(f["lse"], base["lse"], rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        orc.fwd(q, k, v, 0, 1.0, 1, eps=-1e-3)
