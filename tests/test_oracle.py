@@ -129,6 +129,32 @@ def test_one_hot_scores_select_a_value_row():
     np.testing.assert_allclose(f["o"][0], np.broadcast_to(v[0, jstar], (N, d)), atol=1e-20)
 
 
+@pytest.mark.parametrize("causal", [0, 1])
+def test_delta_closed_forms(causal):
+    # delta = rowsum(dO o O) (section 3.4.2, "Failure is linked to the
+    # computation of delta"), where O is known in closed form: the mean of the
+    # visible values when every score is equal, and one value row when a single
+    # key dominates
+    rng = np.random.default_rng(4)
+    BH, N, d = 2, 23, 8
+    k = _rand_bf16(rng, (BH, N, d))
+    v = _rand_bf16(rng, (BH, N, d))
+    g = _rand_bf16(rng, (BH, N, d))
+    f = orc.fwd(np.zeros((BH, N, d), np.float32), k, v, causal, 0.5, 0, dout=g)
+    for i in range(N):
+        n = i + 1 if causal else N
+        mean_v = v[:, :n].astype(np.float64).mean(1)
+        want = (g[:, i].astype(np.float64) * mean_v).sum(1)
+        np.testing.assert_allclose(f["delta"][:, i], want, rtol=0, atol=1e-12)
+    q = np.zeros((BH, N, d), np.float32)
+    q[:, :, 0] = 8.0
+    k2 = _rand_bf16(rng, (BH, N, d), 0.01)
+    k2[:, 0] = [16.0] + [0.0] * (d - 1)     # key 0 is visible to every row and dominates
+    f = orc.fwd(q, k2, v, causal, 0.5, 0, dout=g)
+    want = np.einsum("bnc,bc->bn", g.astype(np.float64), v[:, 0].astype(np.float64))
+    np.testing.assert_allclose(f["delta"], want, rtol=0, atol=1e-12)
+
+
 def test_causal_first_row_is_first_value_row():
     rng = np.random.default_rng(3)
     BH, N, d = 3, 20, 8
