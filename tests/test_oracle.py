@@ -326,6 +326,26 @@ def test_emulation_single_tile_stabilised_has_no_unit_probability():
     np.testing.assert_array_equal(e1["o"][~tied], e0["o"][~tied])
 
 
+@pytest.mark.parametrize("beta", [2.0, 4.0, 8.0])
+def test_emulation_largest_probability_follows_beta(beta):
+    # "What each line does": on a row with a repeated maximum rm > 0 the largest
+    # exponent becomes -(beta-1)*rm, on one with rm < 0 it stays rm (m = 0).  The
+    # emulation's largest BF16 Pbar of such a row is that exponential, up to
+    # BF16 rounding.
+    c, (q, k, v) = _tiny_arrays()
+    ex = orc.fwd(q, k, v, 1, c.scale, 0)
+    em = orc.fwd_emul(q, k, v, 1, c.scale, 1, beta=beta, block_n=c.N)
+    s_max = np.array([[max(q[b, i].astype(np.float64) @ k[b, j].astype(np.float64) for j in range(i + 1))
+                       for i in range(c.N)] for b in range(q.shape[0])])
+    rmz = c.scale * s_max
+    tied = ex["ties"] > 1
+    pos, neg = tied & (rmz > 2.0 ** -4), tied & (rmz < -(2.0 ** -4))
+    assert pos.sum() > 20 and neg.sum() >= 1
+    want = np.where(rmz > 0, np.exp(-(beta - 1.0) * rmz), np.exp(rmz))
+    for sel in (pos, neg):
+        np.testing.assert_allclose(em["p_max"][sel], want[sel], rtol=2.0 ** -8, atol=0)
+
+
 @pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("block_n", [16, 128])
 def test_emulation_output_is_within_bf16_error_of_exact(mode, block_n):
