@@ -140,7 +140,7 @@ class ClockSampler:
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
         if self.gpu_index is not None:
             cmd += ["-i", str(self.gpu_index)]
         try:
@@ -300,8 +300,8 @@ def run_ours(args):
     bwd_timed = fa.fa_bwd_noalloc if ws_bytes <= fa.NOALLOC_SCRATCH_BYTES else fa.fa_bwd
     bwd_name = "fa_bwd_noalloc" if bwd_timed is fa.fa_bwd_noalloc else "fa_bwd"
     for _ in range(args.warmup):
-        flush.zero_()
         for _, m in MODES:
+            flush.zero_()
             one_mode(m, bwd=bwd_timed)
     torch.cuda.synchronize()
     if fa.fa_device_status() != 0:
@@ -315,7 +315,7 @@ def run_ours(args):
     # K steps, launched once right after; it gives the per-kernel durations.
     # Where capture is unavailable the steps are launched call by call.
     def capture(kernel_events):
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(MODES) + 1)]
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * len(MODES))]
                for _ in range(args.steps)]
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
@@ -324,11 +324,11 @@ def run_ours(args):
         try:
             with torch.cuda.graph(g, stream=cap):
                 for s in range(args.steps):
-                    flush.zero_()
-                    evs[s][0].record(cap)
                     for i, (_, m) in enumerate(MODES):
+                        flush.zero_()       # every mode starts with a cold L2
+                        evs[s][2 * i].record(cap)
                         one_mode(m, st=cap, bwd=bwd_timed)
-                        evs[s][i + 1].record(cap)
+                        evs[s][2 * i + 1].record(cap)
         except Exception:
             if kernel_events:
                 fa.fa_profile_stop()
@@ -346,7 +346,7 @@ def run_ours(args):
     except Exception as exc:  # noqa: BLE001 - any capture failure falls back to eager launches
         graph = graph_k = ev_k = None
         timing = f"eager launches (graph capture unavailable: {type(exc).__name__})"
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(MODES) + 1)] for _ in range(args.steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(MODES))] for _ in range(args.steps)]
     torch.cuda.synchronize()
     gpu_index = None
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -364,6 +364,14 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     if graph is not None:
+        # Untimed launches of the same graph for about half a second first, so
+        # that the clock sampler sees the GPU under this load (the timed launch
+        # itself can be shorter than the sampling interval); the timed launch
+        # below overwrites every event these record.
+        t_pre = time.time()
+        while time.time() - t_pre < 0.5:
+            graph.replay()
+            torch.cuda.synchronize()
         for _, m in MODES:                  # every output must come from the graph launch
             for kname in ("dq", "dk", "dv"):
                 outs[m][kname].fill_(float("nan"))
@@ -374,12 +382,12 @@ def run_ours(args):
         graph_k.replay()                    # the same K steps with an event pair per kernel
     else:
         for s in range(args.steps):
-            flush.zero_()                       # L2 flushed between steps, outside the events
             e = ev[s]
-            e[0].record(stream)
             for i, (_, m) in enumerate(MODES):
+                flush.zero_()                   # L2 flushed before every mode, outside the events
+                e[2 * i].record(stream)
                 one_mode(m, bwd=bwd_timed)
-                e[i + 1].record(stream)
+                e[2 * i + 1].record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -391,7 +399,7 @@ def run_ours(args):
     per_mode_ms = [0.0] * len(MODES)
     for e in ev:
         for i in range(len(MODES)):
-            per_mode_ms[i] += e[i].elapsed_time(e[i + 1])
+            per_mode_ms[i] += e[2 * i].elapsed_time(e[2 * i + 1])
     graph = graph_k = None                  # release the graphs before the events they record
     total_ms = max_over_ranks(sum(per_mode_ms), dist, dev)
     ms_step = total_ms / args.steps
@@ -434,6 +442,36 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = world * flop_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
+    # ------------------------------------------- fa_bwd against fa_bwd_noalloc --
+    # The same backward through both entry points, called eagerly one by one
+    # (fa_bwd allocates its workspace from the stream's pool, clears its
+    # barrier words and frees it; fa_bwd_noalloc uses the static scratch),
+    # each bracketed by events right after a forward keeps the GPU busy.
+    alloc_cmp = None
+    if ws_bytes <= fa.NOALLOC_SCRATCH_BYTES:
+        tot = {"fa_bwd": 0.0, "fa_bwd_noalloc": 0.0}
+        n_cmp = max(5, args.steps // 2)
+        for s in range(n_cmp + 2):
+            for bname, bfn in (("fa_bwd", fa.fa_bwd), ("fa_bwd_noalloc", fa.fa_bwd_noalloc)):
+                for _, m in MODES:
+                    b = outs[m]
+                    flush.zero_()
+                    fa.fa_fwd(q, k, v, b["o"], b["lse"], B, H, N, d, causal, scale, m, stream)
+                    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    bfn(q, k, v, b["o"], b["lse"], do, b["dq"], b["dk"], b["dv"], B, H, N, d, causal, scale, m,
+                        stream)
+                    a1.record(stream)
+                    a1.synchronize()
+                    if s >= 2:
+                        tot[bname] += a0.elapsed_time(a1)
+        alloc_cmp = {"fa_bwd_ms": tot["fa_bwd"] / (n_cmp * len(MODES)),
+                     "fa_bwd_noalloc_ms": tot["fa_bwd_noalloc"] / (n_cmp * len(MODES)),
+                     "ratio": tot["fa_bwd"] / tot["fa_bwd_noalloc"], "calls_each": n_cmp * len(MODES),
+                     "how": "eager calls after a forward, events around the backward call, L2 flushed first"}
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("kernel timeout or non-finite output after the timed region")
+
     # ------------------------------------------------------------ roofline --
     peaks, peak_src = load_peaks()
     timed = {kname: v for kname, v in prof.items() if v[0] > 0}
@@ -461,7 +499,7 @@ def run_ours(args):
         "config": {"workload": workload_name(case), "B": B, "H": H, "N": N, "d": d, "causal": causal, "scale": scale,
                    "modes": [n for n, _ in MODES], "planted_tie_rows": 0.05,
                    "flop_per_step": flop_step, "flop_convention": "12*d per visible pair per mode",
-                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "l2": "flushed before every mode's fwd+bwd (256 MiB write, outside the timed events)",
                    "timing": timing},
         "frac_of_peak": value / world / float(peaks["bf16_tflops"]),
         "peak_source": f"bf16_tflops {peaks['bf16_tflops']} ({peak_src})",
@@ -469,6 +507,7 @@ def run_ours(args):
                          "tflops": flop_mode / (per_mode_ms[i] / args.steps * 1e-3) / 1e12}
                      for i, (n, _) in enumerate(MODES)},
         "stabilised_overhead": per_mode_ms[1] / per_mode_ms[0] - 1.0,
+        "bwd_alloc_vs_noalloc": alloc_cmp,
         "roofline": roof,
         "kernels": kernel_share,
         "gpu_launches": gpu_launches,

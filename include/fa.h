@@ -67,7 +67,9 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2, /* d not in {64,128}, or the current device is not sm_103 */
     FA_ERR_ALLOC = 3,       /* a workspace allocation failed */
     FA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map) */
-    FA_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (fa_device_status) */
+    FA_ERR_TIMEOUT = 5,     /* a kernel gave up on a bounded wait (fa_device_status) */
+    FA_ERR_NONFINITE = 6    /* a forward produced a row whose LSE (so its output) is not
+                               finite (fa_device_status) */
 } fa_status_t;
 
 /*
@@ -122,9 +124,18 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * (BF16 in modes 0/1, FP32 in mode 2), dP = dO V^T, dS = scale * P o (dP -
  * delta), dQ = dS K (sections 3.4.2-3.4.3), dK = dS^T Q, dV = P^T dO.
  * Reads q, k, v, o, lse, dO; writes dq, dk, dv (BF16, FP32 accumulation).
- * Allocates a stream-ordered workspace of B*H*N*d*4 + 2*B*H*ceil(N/128)*128*4
- * bytes (cudaMallocAsync on `stream`, freed on `stream` before return);
- * FA_ERR_ALLOC if that fails.
+ * Allocates a stream-ordered workspace (cudaMallocAsync on `stream`, freed on
+ * `stream` before return; FA_ERR_ALLOC if that fails) of Z + R bytes, where
+ * Z = 256 + ceil(B*H*ceil(N/128)*16 / 256)*256 + B*H*N*d*4 (grid-barrier
+ * words, dQ tile counts, FP32 dQ accumulator; cleared with cudaMemsetAsync)
+ * and R = 2*B*H*ceil(N/128)*128*4 (per-row LSE and delta terms).  The first time a workspace size is seen on a
+ * device, the release threshold of the device's current memory pool is raised
+ * to at least that size (never lowered), so steady-state calls reuse pool
+ * memory instead of returning it to the OS at every synchronisation.
+ * The kernel is a persistent, cooperative launch of at most one CTA per SM
+ * whose CTAs synchronise across the grid (a bounded wait, FA_ERR_TIMEOUT if
+ * it runs out); it must be able to have all its CTAs resident at once, which
+ * fails to launch (FA_ERR_CUDA) under an SM partition smaller than the grid.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, void* dq, void* dk, void* dv,
@@ -169,16 +180,20 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
  * Instead of a cudaMallocAsync workspace it uses a fixed scratch array
  * compiled into this library, FA_NOALLOC_SCRATCH_BYTES (32 MiB) per device;
  * every GPU that loads the library holds that array until the process exits.
- * The caller still passes all inputs and outputs.  The call needs
- * B*H*N*d*4 + 2*B*H*ceil(N/128)*128*4 bytes of scratch; larger problems are
- * rejected with FA_ERR_INVALID_ARG before anything is enqueued (fa_last_error
- * says why).  The first call on a device also looks up the array's device
- * address on that device; make that first call before any stream capture.
- * All calls share the one array and it keeps the previous call's contents
- * (the backward's first kernel clears what must start at zero), so calls
- * whose execution overlaps on the GPU -- e.g. on two streams without an
- * ordering between them -- race on the scratch and give wrong results:
- * serialise them.  Allocates nothing and calls no allocating routine.
+ * The caller still passes all inputs and outputs.  The array is split into a
+ * 30 MiB part that holds fa_bwd's Z bytes (see fa_bwd) and a 2 MiB part that
+ * holds its R bytes; problems whose Z or R does not fit (at d = 64, B*H*N
+ * above about 122,000 rows) are rejected with FA_ERR_INVALID_ARG before
+ * anything is enqueued (fa_last_error says why).  Each call leaves the 30 MiB
+ * part at zero again, so no clearing is enqueued.  The first call on a device also looks up the
+ * array's device address on that device; make that first call before any
+ * stream capture (a first call made while `stream` is capturing is refused
+ * with FA_ERR_INVALID_ARG).  All calls share the one array and it keeps the
+ * previous call's contents (a call that timed out may leave the 30 MiB part
+ * dirty: fa_device_status with reset clears it), so calls whose execution
+ * overlaps on the GPU -- e.g. on two streams without an ordering between them
+ * -- race on the scratch and give wrong results: serialise them.  Allocates
+ * nothing and calls no allocating routine.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -232,8 +247,12 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o,
 /*
  * fa_device_status -- synchronises `stream`, then returns FA_ERR_TIMEOUT if any
  * kernel of this library on the current device recorded a bounded-wait
- * timeout since the last reset, FA_ERR_CUDA if the synchronisation failed,
- * else FA_OK.  reset != 0 clears the recorded status.
+ * timeout since the last reset, else FA_ERR_NONFINITE if a forward wrote a
+ * row whose LSE is not finite (every Pbar of the row underflowed, e.g. a large
+ * beta on a large repeated maximum; its O is then not finite either),
+ * FA_ERR_CUDA if the synchronisation failed, else FA_OK.  reset != 0 clears
+ * the recorded status (and, after a timeout, the allocation-free backward's
+ * grid-barrier words).
  */
 int fa_device_status(fa_stream_t stream, int reset);
 
@@ -256,9 +275,10 @@ int fa_device_status(fa_stream_t stream, int reset);
 enum {
     FA_KERNEL_FWD = 0,       /* forward (modes 0-2) */
     FA_KERNEL_FWD_STATS = 1, /* forward replay writing tie counts */
-    FA_KERNEL_BWD_PRE = 2,   /* delta, LSE*log2(e), dQ accumulator zeroing */
-    FA_KERNEL_BWD_MAIN = 3,  /* the five-MMA backward */
-    FA_KERNEL_DQ_CONVERT = 4,/* FP32 dQ accumulator -> BF16 */
+    FA_KERNEL_BWD_PRE = 2,   /* reserved: no longer launched (phase A of FA_KERNEL_BWD_MAIN) */
+    FA_KERNEL_BWD_MAIN = 3,  /* the backward: delta and LSE*log2(e) per row, the
+                                five-MMA main loop, FP32 dQ accumulator -> BF16 */
+    FA_KERNEL_DQ_CONVERT = 4,/* reserved: no longer launched (phase C of FA_KERNEL_BWD_MAIN) */
     FA_KERNEL_PV_ERR = 5,    /* CUDA-core reference for pv_err */
     FA_KERNEL_COUNT = 6,
     FA_PROFILE_MAX_LAUNCHES = 65536

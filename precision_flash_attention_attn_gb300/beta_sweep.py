@@ -16,7 +16,12 @@ reports over the rows with a planted tie whose exact tie count is > 1:
                   every Pbar of a row with a large repeated maximum), which the
                   means leave out.
 
-Usage: python -m precision_flash_attention_attn_gb300.beta_sweep [--betas 2,4,8] [--workload ties]
+With --neg-v the workload's V gets the negative-mean columns of the
+invariant fixture (a quarter of the columns from N(-2, 1), seed + 1000), the
+condition under which the paper's bias mechanism acts (section 3.4.4, "Cause
+2"; section 5, the mostly negative V[:, 20]).
+
+Usage: python -m precision_flash_attention_attn_gb300.beta_sweep [--betas 2,4,8] [--workload ties] [--neg-v]
 Prints one JSON line per setting.  Needs a GPU.
 """
 from __future__ import annotations
@@ -44,10 +49,15 @@ def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--betas", default="2,4,8")
     ap.add_argument("--workload", default="ties")
+    ap.add_argument("--neg-v", action="store_true", help="negative-mean V columns (seed + 1000)")
     args = ap.parse_args(argv)
     betas = [float(b) for b in args.betas.split(",") if b.strip()]
 
-    c = make_case(args.workload)
+    if args.neg_v:
+        from .inputs import CASES
+        c = make_case(args.workload, neg_v_cols=True, seed=CASES[args.workload].seed + 1000)
+    else:
+        c = make_case(args.workload)
 
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
@@ -64,8 +74,9 @@ def main(argv=None) -> int:
         fa.fa_tie_stats_ex(q, k, v, o, B, H, N, d, c.causal, c.scale, mode, tc, pe, po, dO=do, delta_err=de,
                            beta=beta)
         finite = torch.isfinite(o.float()).all(-1)
-        if fa.fa_device_status() != 0:
-            raise RuntimeError("kernel timeout")
+        status = fa.fa_device_status()
+        if status not in (0, 6):            # FA_ERR_NONFINITE is counted below, not an error
+            raise RuntimeError(f"device status {fa.fa_status_string(status)}")
         return (tc.cpu().numpy().reshape(-1), pe.cpu().numpy().reshape(-1).astype(np.float64),
                 po.cpu().numpy().reshape(2, -1), de.cpu().numpy().reshape(-1).astype(np.float64),
                 finite.cpu().numpy().reshape(-1))
@@ -79,7 +90,8 @@ def main(argv=None) -> int:
         pv_m, pv_se = _mean_se(pe[ok])
         de_m, de_se = _mean_se(de[ok])
         print(json.dumps({
-            "workload": args.workload, "setting": name, "tied_rows": int(rows.size),
+            "workload": args.workload + (" (negative-mean V)" if args.neg_v else ""), "setting": name,
+            "tied_rows": int(rows.size),
             "p_one0_rows": float((po[0][rows] > 0).mean()) if rows.size else None,
             "p_one1_mean": float(po[1][rows].mean()) if rows.size else None,
             "pv_err": {"mean": pv_m, "se": pv_se}, "delta_err": {"mean": de_m, "se": de_se},

@@ -30,6 +30,8 @@ struct DeviceInfo {
     bool supported = false;
     int* status = nullptr;
     int num_sms = 0;
+    int dev = 0;
+    uint64_t pool_threshold = 0;  // release threshold this library has set on the device's mempool
 };
 
 std::mutex g_mu;
@@ -46,7 +48,10 @@ int device_info(DeviceInfo** out) {
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return cuda_fail("cudaGetDevice", ce);
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= kMaxDevices) {
+        fa::set_error_msg("device_info", "device index exceeds the library's device table (64)");
+        return FA_ERR_UNSUPPORTED;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo& di = g_dev[dev];
     if (!di.probed) {
@@ -64,6 +69,7 @@ int device_info(DeviceInfo** out) {
             if (ce != cudaSuccess) return cuda_fail("cudaGetSymbolAddress(status word)", ce);
             di.status = static_cast<int*>(p);
         }
+        di.dev = dev;
         di.probed = true;
     }
     if (!di.supported) return FA_ERR_UNSUPPORTED;
@@ -130,6 +136,116 @@ int check_params(const fa_stab_params_t* prm, float* beta) {
 
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
+// Backward workspace, two regions:
+//   zero region  [grid barrier words, 256 B][FP32 dQ accumulator BH*N*d]:
+//                must be zero when the kernel starts;
+//   row region   [-LSE*log2e BH*Npad][-alpha*delta BH*Npad]: written by the
+//                kernel itself.
+// Every part starts on a 256-byte boundary (BH*N*d*4 and BH*Npad*4 are
+// multiples of 256).
+constexpr size_t kSyncBytes = 256;
+
+struct BwdSizes {
+    size_t acc, rows;  // accumulator, one of the two row arrays
+    size_t zero_bytes() const { return kSyncBytes + acc; }
+    size_t row_bytes() const { return 2 * rows; }
+};
+
+BwdSizes bwd_sizes(int BH, int N, int d) {
+    const int n_qt = (N + fa::kBlockM - 1) / fa::kBlockM;
+    BwdSizes z;
+    z.acc = static_cast<size_t>(BH) * N * d * sizeof(float);
+    z.rows = static_cast<size_t>(BH) * n_qt * fa::kBlockM * sizeof(float);
+    return z;
+}
+
+bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     const void* dq, const void* dk, const void* dv) {
+    return aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o) && aligned16(lse) && aligned16(dO) &&
+           aligned16(dq) && aligned16(dk) && aligned16(dv);
+}
+
+// Enqueue the backward kernel.  `zero` is the zero region (bwd_sizes layout,
+// all zero), `rows` the row region.  clean = 1 asks the kernel to leave the
+// zero region at zero again.  Arguments are already validated.
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
+                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st) {
+    const int BH = B * H;
+    const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
+    char* zb = static_cast<char*>(zero);
+    uint32_t* sync = reinterpret_cast<uint32_t*>(zb);
+    float* dq_acc = reinterpret_cast<float*>(zb + kSyncBytes);
+    float* lse2 = static_cast<float*>(rows);
+    float* delta = lse2 + static_cast<size_t>(BH) * Npad;
+    CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
+    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
+        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
+        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
+        return FA_ERR_CUDA;
+    fa::BwdArgs a{};
+    a.tm_q = &mq;
+    a.tm_k = &mk;
+    a.tm_v = &mv;
+    a.tm_do = &mdo;
+    a.tm_dqacc = &macc;
+    a.tm_dk = &mdk;
+    a.tm_dv = &mdv;
+    a.o = o;
+    a.lse = lse;
+    a.dout = dO;
+    a.dq_acc = dq_acc;
+    a.lse2 = lse2;
+    a.delta = delta;
+    a.sync = sync;
+    a.clean = clean;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.BH = BH;
+    a.N = N;
+    a.Npad = Npad;
+    a.d = d;
+    a.causal = causal;
+    a.mode = mode;
+    a.scale = scale;
+    a.scale_log2 = log2e_times(scale);
+    a.status = di->status;
+    a.num_sms = di->num_sms;
+    return fa::launch_bwd(a, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Keep at least `bytes` of the current device's stream-ordered pool reserved
+// across synchronisations, so that steady-state workspace allocations are
+// served from the pool instead of the OS.  Only ever raises the threshold.
+void reserve_pool(DeviceInfo* di, size_t bytes) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (di->pool_threshold >= bytes) return;
+    cudaMemPool_t pool;
+    if (cudaDeviceGetMemPool(&pool, di->dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    cuuint64_t cur = 0;
+    if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &cur) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    if (cur < bytes) {
+        cuuint64_t want = bytes;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &want) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        cur = want;
+    }
+    di->pool_threshold = cur;
+}
+
 }  // namespace
 
 namespace fa {
@@ -154,6 +270,7 @@ const char* fa_status_string(int status) {
         case FA_ERR_ALLOC: return "FA_ERR_ALLOC";
         case FA_ERR_CUDA: return "FA_ERR_CUDA";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        case FA_ERR_NONFINITE: return "FA_ERR_NONFINITE";
         default: return "FA_ERR_UNKNOWN";
     }
 }
@@ -200,79 +317,39 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.beta = beta;
     a.status = di->status;
     a.num_sms = di->num_sms;
+    const char* hook = std::getenv("FA_TEST_WITHHOLD_K");
+    a.test_withhold_k = (hook && hook[0] == '1') ? 1 : 0;
     return fa::launch_fwd(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
            fa_stream_t stream) {
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-        return FA_ERR_INVALID_ARG;
+    if (!bwd_pointers_ok(q, k, v, o, lse, dO, dq, dk, dv)) return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
-    const int BH = B * H;
-    const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
-    const size_t acc_bytes = static_cast<size_t>(BH) * N * d * sizeof(float);
-    const size_t row_bytes = static_cast<size_t>(BH) * Npad * sizeof(float);
-    const size_t ws_bytes = acc_bytes + 2 * row_bytes;
+    const BwdSizes z = bwd_sizes(B * H, N, d);
+    const size_t ws_bytes = z.zero_bytes() + z.row_bytes();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    void* ws = nullptr;
     const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
     if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    reserve_pool(di, ws_bytes);
+    void* ws = nullptr;
     cudaError_t ae = cudaMallocAsync(&ws, ws_bytes, st);
     if (ae != cudaSuccess || !ws) {
         fa::set_error("cudaMallocAsync(workspace)", ae);
         cudaGetLastError();
         return FA_ERR_ALLOC;
     }
-    float* dq_acc = static_cast<float*>(ws);
-    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-    float* delta = lse2 + static_cast<size_t>(BH) * Npad;
-
-    CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
-    rc = FA_OK;
-    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
-        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
-        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
-        rc = FA_ERR_CUDA;
-    if (rc == FA_OK) {
-        fa::BwdArgs a{};
-        a.tm_q = &mq;
-        a.tm_k = &mk;
-        a.tm_v = &mv;
-        a.tm_do = &mdo;
-        a.tm_dqacc = &macc;
-        a.tm_dk = &mdk;
-        a.tm_dv = &mdv;
-        a.o = o;
-        a.lse = lse;
-        a.dout = dO;
-        a.dq_acc = dq_acc;
-        a.lse2 = lse2;
-        a.delta = delta;
-        a.dq = dq;
-        a.dk = dk;
-        a.dv = dv;
-        a.BH = BH;
-        a.N = N;
-        a.Npad = Npad;
-        a.d = d;
-        a.causal = causal;
-        a.mode = mode;
-        a.scale = scale;
-        a.scale_log2 = log2e_times(scale);
-        a.status = di->status;
-        a.num_sms = di->num_sms;
-        if (fa::launch_bwd(a, st) != cudaSuccess) rc = FA_ERR_CUDA;
-    }
+    // fresh memory: the barrier words, counts and accumulator start at zero
+    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
+    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
+    if (rc == FA_OK)
+        rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
+                             static_cast<char*>(ws) + z.zero_bytes(), 0, st);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;
@@ -309,6 +386,10 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
         return FA_ERR_ALLOC;
     }
     float* o32 = static_cast<float*>(ws);
+    // lse32 only receives the forward's LSE output, which the call requires.
+    // The backward below takes the caller's lse on purpose: P is recomputed
+    // from the same LSE as in the stored-O backward, so only delta's source
+    // differs between the two.
     float* lse32 = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
     rc = fa_fwd_ex(q, k, v, o32, lse32, B, H, N, d, causal, scale, FA_MODE_FP32_OUT, nullptr, stream);
     if (rc == FA_OK) rc = fa_bwd(q, k, v, o32, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, FA_MODE_FP32_OUT, stream);
@@ -322,20 +403,35 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+// fixed split: the zero region first, the row region in the last 2 MiB
+constexpr size_t kNoallocRowBytes = 2u * 1024u * 1024u;
+constexpr size_t kNoallocZeroBytes = FA_NOALLOC_SCRATCH_BYTES - kNoallocRowBytes;
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
 
 // Device address of the scratch array on the current device.  In host code
 // g_noalloc_scratch names a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
-int noalloc_scratch(void** out) {
+// cudaGetSymbolAddress, once per device, with that device current.  That
+// lookup must not happen inside a stream capture, so a first call on a device
+// made while `stream` is capturing is refused.
+int noalloc_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    if (dev < 0 || dev >= kMaxDevices) {
+        fa::set_error_msg("fa_bwd_noalloc", "device index exceeds the library's device table (64)");
+        return FA_ERR_UNSUPPORTED;
+    }
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_addr[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cudaGetLastError();
+            fa::set_error_msg("fa_bwd_noalloc",
+                              "the first call on a device looks up the scratch address and must precede stream capture");
+            return FA_ERR_INVALID_ARG;
+        }
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) return cuda_fail("cudaGetSymbolAddress(scratch)", e);
@@ -352,68 +448,28 @@ extern "C" {
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
                    fa_stream_t stream) {
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-        return FA_ERR_INVALID_ARG;
+    if (!bwd_pointers_ok(q, k, v, o, lse, dO, dq, dk, dv)) return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
-    const int BH = B * H;
-    const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
-    const size_t acc_bytes = static_cast<size_t>(BH) * N * d * sizeof(float);
-    const size_t row_bytes = static_cast<size_t>(BH) * Npad * sizeof(float);
-    const size_t ws_bytes = acc_bytes + 2 * row_bytes;
-    if (ws_bytes > FA_NOALLOC_SCRATCH_BYTES) {
-        char msg[160];
-        snprintf(msg, sizeof msg, "needs %zu bytes of scratch, the static limit is %u bytes", ws_bytes,
-                 FA_NOALLOC_SCRATCH_BYTES);
+    const BwdSizes z = bwd_sizes(B * H, N, d);
+    if (z.zero_bytes() > kNoallocZeroBytes || z.row_bytes() > kNoallocRowBytes) {
+        char msg[200];
+        snprintf(msg, sizeof msg,
+                 "needs %zu + %zu bytes of scratch, the static limit is %zu + %zu bytes (FA_NOALLOC_SCRATCH_BYTES)",
+                 z.zero_bytes(), z.row_bytes(), kNoallocZeroBytes, kNoallocRowBytes);
         fa::set_error_msg("fa_bwd_noalloc", msg);
         return FA_ERR_INVALID_ARG;
     }
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     void* ws = nullptr;
-    if ((rc = noalloc_scratch(&ws))) return rc;
-    float* dq_acc = static_cast<float*>(ws);
-    float* lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + acc_bytes);
-    float* delta = lse2 + static_cast<size_t>(BH) * Npad;
-
-    CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
-    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
-        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
-        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
-        return FA_ERR_CUDA;
-    fa::BwdArgs a{};
-    a.tm_q = &mq;
-    a.tm_k = &mk;
-    a.tm_v = &mv;
-    a.tm_do = &mdo;
-    a.tm_dqacc = &macc;
-    a.tm_dk = &mdk;
-    a.tm_dv = &mdv;
-    a.o = o;
-    a.lse = lse;
-    a.dout = dO;
-    a.dq_acc = dq_acc;
-    a.lse2 = lse2;
-    a.delta = delta;
-    a.dq = dq;
-    a.dk = dk;
-    a.dv = dv;
-    a.BH = BH;
-    a.N = N;
-    a.Npad = Npad;
-    a.d = d;
-    a.causal = causal;
-    a.mode = mode;
-    a.scale = scale;
-    a.scale_log2 = log2e_times(scale);
-    a.status = di->status;
-    a.num_sms = di->num_sms;
-    return fa::launch_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    if ((rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &ws))) return rc;
+    // The zero region is zero from load time and every completed call leaves
+    // it so (clean = 1); fa_device_status clears it after a timeout.  The row
+    // region sits apart from it, at the end of the array, so that a call with
+    // other sizes never finds row values where it needs zeros.
+    return launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
+                           static_cast<char*>(ws) + kNoallocZeroBytes, 1, static_cast<cudaStream_t>(stream));
 }
 
 int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
@@ -491,8 +547,17 @@ int fa_device_status(fa_stream_t stream, int reset) {
     if (reset && h != 0) {
         const int zero = 0;
         if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+        // a launch that gave up may have left the allocation-free backward's
+        // zero region (barrier words, counts, accumulator) dirty
+        void* scratch = nullptr;
+        {
+            std::lock_guard<std::mutex> lk(g_noalloc_mu);
+            scratch = g_noalloc_addr[di->dev];
+        }
+        if (scratch && cudaMemset(scratch, 0, kNoallocZeroBytes) != cudaSuccess) return FA_ERR_CUDA;
     }
-    return h == 0 ? FA_OK : FA_ERR_TIMEOUT;
+    if (h & 1) return FA_ERR_TIMEOUT;
+    return h == 0 ? FA_OK : FA_ERR_NONFINITE;
 }
 
 }  // extern "C"

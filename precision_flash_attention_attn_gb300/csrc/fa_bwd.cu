@@ -9,30 +9,29 @@
 //   dS    = alpha * P o (dP - delta)
 //   dQ    = dS K,   dK = dS^T Q,   dV = P^T dO   (dK, dV: textbook gradients)
 //
-// Kernels, in stream order:
-//   bwd_pre_kernel   -LSE*log2(e) and -alpha*delta per row into padded
-//                    workspaces, zero the FP32 dQ accumulator.
-//   bwd_kernel       one CTA per (batch*head, 128-key tile); K and V stay in
-//                    shared memory while the CTA walks the 128-query tiles
-//                    (causal: only tiles at or below the diagonal).  Per query
-//                    tile, five tcgen05 MMAs:
-//                      S^T  = K Q^T      (TMEM, FP32)
-//                      dP^T = V dO^T     (TMEM, FP32)
-//                      dV  += P^T dO     (TMEM accumulator)
-//                      dK  += dS^T Q     (TMEM accumulator)
-//                      dQ_t = dS K       (TMEM), added to the FP32 workspace
-//                                        with TMA reduce-add
-//                    Warp roles: two math warpgroups (warps 0-3: query
-//                    columns 0-63 of the tile, warps 4-7: columns 64-127;
-//                    thread t of a warpgroup owns key row t) recompute P^T and
-//                    dS^T; a drain warpgroup (warps 8-11, one TMEM lane
-//                    quarter each) moves each dQ tile from TMEM into the
-//                    reduce-add and each item's dK and dV from TMEM to HBM
-//                    (TMA stores), off the math chain;
-//                    warp 12 issues TMA loads; warp 13 issues the MMAs.  The
-//                    next tile's S^T and dP^T are issued ahead of the current
-//                    tile's dK/dQ products.
-//   dq_convert_kernel  dQ workspace (FP32) -> BF16.
+// One persistent kernel, one CTA per SM (the launch is cooperative: all CTAs
+// are resident at once):
+//   A  every thread: -LSE*log2(e) and -alpha*delta per row into padded
+//      workspaces (delta from the stored O of the mode), then a grid barrier.
+//   B  work items (batch*head, 128-key tile); K and V stay in shared memory
+//      while the CTA walks the 128-query tiles (causal: only tiles at or below
+//      the diagonal).  Per query tile, five tcgen05 MMAs:
+//        S^T  = K Q^T      (TMEM, FP32)
+//        dP^T = V dO^T     (TMEM, FP32)
+//        dV  += P^T dO     (TMEM accumulator)
+//        dK  += dS^T Q     (TMEM accumulator)
+//        dQ_t = dS K       (TMEM), added to the FP32 accumulator with TMA
+//                          reduce-add
+//      Warp roles: two math warpgroups (warps 0-3: query columns 0-63 of the
+//      tile, warps 4-7: columns 64-127; thread t of a warpgroup owns key row
+//      t) recompute P^T and dS^T; a drain warpgroup (warps 8-11, one TMEM lane
+//      quarter each) moves each dQ tile from TMEM into the reduce-add and each
+//      item's dK and dV from TMEM to HBM (TMA stores), off the math chain;
+//      warp 12 issues TMA loads; warp 13 issues the MMAs.  The next tile's S^T
+//      and dP^T are issued ahead of the current tile's dK/dQ products.
+//   C  once every CTA's reduce-adds have landed (a grid barrier), the math
+//      warps convert the FP32 dQ accumulator to BF16 (and, when asked, write
+//      zeros back, leaving the accumulator ready for the next call).
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -43,67 +42,73 @@
 namespace fa {
 namespace {
 
-// ------------------------------------------------------------- preprocess --
+struct BwdParams {
+    const void* o;        // [BH, N, d] BF16, or FP32 in mode 2
+    const float* lse;     // [BH, N]
+    const void* dout;     // [BH, N, d] BF16
+    float* dq_acc;        // FP32 [BH, N, d] accumulator
+    void* dq;             // [BH, N, d] BF16 output
+    float* lse2;          // [BH, Npad]: -LSE*log2(e), -inf on padded rows
+    float* delta;         // [BH, Npad]: -alpha*rowsum(dO o O), 0 on padded rows
+    uint32_t* sync;       // grid barrier words (zero before the first launch)
+    int clean;            // 1: leave the accumulator and the barrier words at zero afterwards
+    int BH, N, Npad, mode;
+    int n_kt;     // key tiles per (batch, head)
+    int n_items;  // BH * n_kt
+    float scale, scale_log2;
+    int* status;
+};
 
-// D/8 threads per row, 8 elements (16 bytes of dO) each; rows padded to Npad.
-// Each warp works on kUnroll groups of rows at once so that enough loads are
-// in flight to keep HBM busy.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
-    constexpr int TPR = D / 8;       // threads per row
-    constexpr int RPW = 32 / TPR;    // rows per warp and group
-    constexpr int kUnroll = 4;
-    const int lane = threadIdx.x & 31;
-    const int sub = lane % TPR;
-    // The first half of the blocks compute the rows, the second half clear the
-    // dQ accumulator, so reads and writes proceed side by side.
-    const int row_blocks = static_cast<int>(gridDim.x) / 2;
-    if (static_cast<int>(blockIdx.x) >= row_blocks) {
-        const size_t n4 = static_cast<size_t>(a.BH) * a.N * D / 4;
-        float4* acc4 = reinterpret_cast<float4*>(a.dq_acc);
-        const size_t nthr = static_cast<size_t>(gridDim.x - row_blocks) * blockDim.x;
-        const size_t tid = static_cast<size_t>(blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
-        for (size_t e = tid; e < n4; e += 4 * nthr) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (e + u * nthr < n4) acc4[e + u * nthr] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        return;
-    }
+constexpr int kBwdThreads = 512;
+constexpr uint32_t kBarDrained = 1;  // named barrier: the drain warps' reduce-adds have landed (math + drain)
+constexpr uint32_t kBarMath = 2;     // named barrier: the math warps
+
+// ------------------------------------------------------------- phase A ----
+// D/8 threads per row, 8 elements (16 bytes of dO) each; each thread takes
+// kUnroll rows, a grid stride apart, per step, and every load of a step (dO,
+// O and the LSE) is issued before any is used, so a step costs one memory
+// round trip.  O32: O is FP32 (mode 2).
+template <int D, bool O32>
+__device__ __forceinline__ void prepare_rows(const BwdParams& p) {
+    constexpr int TPR = D / 8;                  // threads per row
+    constexpr int RPC = kBwdThreads / TPR;      // rows per CTA and step
+    constexpr int kUnroll = O32 ? 5 : 7;
+    const int tid = threadIdx.x;
+    const int sub = tid % TPR;
     // rows < 2^31 (BH * Npad * d is checked against it), so 32-bit index math
-    const int rows = a.BH * a.Npad;
-    const int nwarps = row_blocks * (blockDim.x >> 5);
-    const int gw = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int rows = p.BH * p.Npad;
+    const int stride = static_cast<int>(gridDim.x) * RPC;
     const float log2e = 1.4426950408889634f;
-    for (int r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
+    for (int r0 = static_cast<int>(blockIdx.x) * RPC + tid / TPR; r0 < rows; r0 += kUnroll * stride) {
         uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
+        float lse[kUnroll];
         bool valid[kUnroll];
-        int r[kUnroll], bhs[kUnroll], is[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            r[u] = r0 + u * RPW + lane / TPR;
-            const int bh = r[u] / a.Npad;
-            const int i = r[u] - bh * a.Npad;
-            bhs[u] = bh;
-            is[u] = i;
-            valid[u] = r[u] < rows && i < a.N;
+            const int r = r0 + u * stride;
+            const int bh = r / p.Npad;
+            const int i = r - bh * p.Npad;
+            valid[u] = r < rows && i < p.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
+            lse[u] = 0.f;
             if (valid[u]) {
-                const size_t base = (static_cast<size_t>(bh) * a.N + i) * D + sub * 8;
-                g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + base);
-                if (a.mode == 2) {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(a.o) + base);
-                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(a.o) + base + 4);
+                const size_t row = static_cast<size_t>(bh) * p.N + i;
+                const size_t base = row * D + sub * 8;
+                g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
+                if (O32) {
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.o) + base);
+                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.o) + base + 4);
                 } else {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + base);
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + base);
                 }
+                if (sub == 0) lse[u] = p.lse[row];
             }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const uint32_t gw4[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
             float acc = 0.f;
-            if (a.mode == 2) {
+            if (O32) {
                 const uint32_t of[8] = {o[u].x, o[u].y, o[u].z, o[u].w, o2[u].x, o2[u].y, o2[u].z, o2[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -120,34 +125,37 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
             }
 #pragma unroll
             for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (sub == 0 && r[u] < rows) {
-                const int bh = bhs[u];
-                const int i = is[u];
-                // stored pre-negated / pre-scaled for the main kernel's FMAs:
+            const int r = r0 + u * stride;
+            if (sub == 0 && r < rows) {
+                // stored pre-negated / pre-scaled for the main phase's FMAs:
                 //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
                 //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
-                a.delta[r[u]] = valid[u] ? -a.scale * acc : 0.f;
+                p.delta[r] = valid[u] ? -p.scale * acc : 0.f;
                 // padded rows: P = exp2(s - inf) = 0
-                a.lse2[r[u]] = valid[u] ? -a.lse[static_cast<size_t>(bh) * a.N + i] * log2e : -INFINITY;
+                p.lse2[r] = valid[u] ? -lse[u] * log2e : -INFINITY;
             }
         }
     }
 }
 
-// dQ workspace (FP32) -> BF16, eight elements per thread and step, four
-// steps' loads in flight.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
-                                                         size_t n8) {
-    const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
-    const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+// ------------------------------------------------------------- phase C ----
+// dQ accumulator (FP32) -> BF16 by threads 0..nthreads_cta-1 of every CTA,
+// eight elements per thread and step, four steps' loads in flight; with
+// `clean` the accumulator is zeroed as it is read.  The loads bypass L1: the
+// accumulator was written by other SMs' reduce-adds during this launch.
+__device__ __forceinline__ void convert_dq(const BwdParams& p, size_t n8, int nthreads_cta) {
+    float4* acc = reinterpret_cast<float4*>(p.dq_acc);
+    uint4* dq = reinterpret_cast<uint4*>(p.dq);
+    const size_t nthr = static_cast<size_t>(gridDim.x) * nthreads_cta;
+    const size_t tid = static_cast<size_t>(blockIdx.x) * nthreads_cta + threadIdx.x;
     for (size_t e0 = tid; e0 < n8; e0 += 4 * nthr) {
         float4 x[4], y[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const size_t e = e0 + u * nthr;
             if (e < n8) {
-                x[u] = reinterpret_cast<const float4*>(acc)[2 * e];
-                y[u] = reinterpret_cast<const float4*>(acc)[2 * e + 1];
+                x[u] = __ldcg(acc + 2 * e);
+                y[u] = __ldcg(acc + 2 * e + 1);
             }
         }
 #pragma unroll
@@ -159,7 +167,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
                 w.y = pack_bf16x2(x[u].z, x[u].w);
                 w.z = pack_bf16x2(y[u].x, y[u].y);
                 w.w = pack_bf16x2(y[u].z, y[u].w);
-                reinterpret_cast<uint4*>(dq)[e] = w;
+                dq[e] = w;
+                if (p.clean) {
+                    acc[2 * e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    acc[2 * e + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
     }
@@ -207,6 +219,7 @@ struct BwdLayout {
     static constexpr int kDrain = kAccFree + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
+    static constexpr int kFlag = kTmemSlot + 8;   // phase C go-ahead (the grid barrier's verdict)
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kAlloc <= 232448, "shared memory budget");
@@ -224,21 +237,11 @@ struct BwdLayout {
     static constexpr int kDrainWarp0 = 8;
     static constexpr int kProducerWarp = 12;
     static constexpr int kMmaWarp = 13;            // warps 14, 15 idle (whole warpgroups for setmaxnreg)
-    static constexpr int kThreads = 512;
+    static constexpr int kThreads = kBwdThreads;
     // registers: 2 x 128 x 168 (math) + 2 x 128 x 88 (drain, producer, MMA) = 512 x 128
     static constexpr uint32_t kRegsMath = 168;
     static constexpr uint32_t kRegsOther = 88;
     static_assert(256 * kRegsMath + 256 * kRegsOther == kThreads * 128, "register split");
-};
-
-struct BwdParams {
-    float* lse2;
-    float* delta;
-    int BH, N, Npad;
-    int n_kt;     // key tiles per (batch, head)
-    int n_items;  // BH * n_kt
-    float scale, scale_log2;
-    int* status;
 };
 
 // Work items are (key tile, batch-head) pairs numbered longest first (causal:
@@ -305,6 +308,16 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
+    // Phase A.  Nothing above reads or writes global memory, so under
+    // programmatic dependent launch all of it overlaps the previous kernel.
+    griddep_wait();
+    if (p.mode == 2)
+        prepare_rows<D, true>(p);
+    else
+        prepare_rows<D, false>(p);
+    const bool started = grid_barrier(p.sync, p.status);
+
+    if (started) {
     if (warp >= L::kDrainWarp0) {
     regs_dec<L::kRegsOther>();
     if (warp == L::kProducerWarp) {
@@ -611,7 +624,15 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 }
             }
         }
-        if (lane == 0) bulk_wait0();
+        // every reduce-add has landed (not only read its staging buffer)
+        // before the grid barrier that precedes phase C's reads
+        if (lane == 0) {
+            bulk_wait0();
+            fence_async_global();
+            __threadfence();
+        }
+        __syncwarp();
+        named_arrive(kBarDrained, L::kMathThreads + L::kDrainThreads);
     }
     } else {
     regs_inc<L::kRegsMath>();
@@ -747,7 +768,22 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             }
         }
     }
+    // ------------------------------------------------------------ phase C
+    // The math warps convert the dQ accumulator once the drain warps of every
+    // CTA have seen their reduce-adds land.  (Done in this branch, within its
+    // register budget: no register hand-back is needed.)
+    named_sync(kBarDrained, L::kMathThreads + L::kDrainThreads);
+    if (threadIdx.x == 0) {
+        const bool drained = grid_arrive_wait(p.sync, p.status);
+        *reinterpret_cast<volatile int*>(smem + L::kFlag) = drained ? 1 : 0;
     }
+    named_sync(kBarMath, L::kMathThreads);
+    fence_async_global();
+    griddep_launch_dependents();
+    if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
+        convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads);
+    }
+    }  // started
 
     tc_fence_before();
     __syncthreads();
@@ -768,8 +804,16 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
         return e;
     }
     BwdParams p;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.dout = a.dout;
+    p.dq_acc = a.dq_acc;
+    p.dq = a.dq;
     p.lse2 = a.lse2;
     p.delta = a.delta;
+    p.sync = a.sync;
+    p.clean = a.clean;
+    p.mode = a.mode;
     p.BH = a.BH;
     p.N = a.N;
     p.Npad = a.Npad;
@@ -778,13 +822,26 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
-    // persistent: one CTA per SM (or per item, if fewer)
+    // persistent: one CTA per SM (or per item, if fewer), all resident at once
+    // for the grid barriers (cooperative launch); programmatic dependent
+    // launch lets the set-up overlap the previous kernel in the stream
     const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     prof_begin(3, stream);
-    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
+    e = cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
     prof_end(3, stream);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFuncAttributes fa_attr{};
         char msg[200];
@@ -799,40 +856,11 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     return e;
 }
 
-int num_sms() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 148;
-}
-
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-    const int sms = num_sms();
-    prof_begin(2, stream);
-    if (a.d == 64)
-        bwd_pre_kernel<64><<<sms * 8, 256, 0, stream>>>(a);
-    else
-        bwd_pre_kernel<128><<<sms * 8, 256, 0, stream>>>(a);
-    prof_end(2, stream);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        set_error("bwd_pre launch", e);
-        return e;
-    }
-    if (a.d == 64)
-        e = a.causal ? launch_main<64, true>(a, stream) : launch_main<64, false>(a, stream);
-    else
-        e = a.causal ? launch_main<128, true>(a, stream) : launch_main<128, false>(a, stream);
-    if (e != cudaSuccess) return e;
-    const size_t n8 = static_cast<size_t>(a.BH) * a.N * a.d / 8;
-    prof_begin(4, stream);
-    dq_convert_kernel<<<sms * 8, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n8);
-    prof_end(4, stream);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) set_error("dq_convert launch", e);
-    return e;
+    if (a.d == 64) return a.causal ? launch_main<64, true>(a, stream) : launch_main<64, false>(a, stream);
+    return a.causal ? launch_main<128, true>(a, stream) : launch_main<128, false>(a, stream);
 }
 
 }  // namespace fa

@@ -115,6 +115,7 @@ struct FwdParams {
     float scale_log2;
     float beta;   // mode 1: shift factor of rows with a positive repeated maximum
     int* status;
+    int test_withhold_k;  // test hook (see FwdArgs)
 };
 
 // Work items are (query-tile group, batch-head) pairs, numbered longest first
@@ -194,6 +195,9 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+    // Nothing above reads or writes global memory, so under programmatic
+    // dependent launch all of it overlaps the previous kernel in the stream.
+    griddep_wait();
 
     if (warp >= kProducerWarp) {
         if (NQ == 2) regs_dec<L::kRegsOther>();
@@ -235,10 +239,15 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                             for (int t = 0; t < NQ && ok; ++t)
                                 ok = mbar_wait(bar(L::kKVEmpty + t * S + s), (u - 1) & 1u, p.status);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
-                        for (int b = 0; b < D / 64; ++b)
-                            tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
-                                        b * 64, j * kBlockN, bh);
+                        // test hook: CTA 0 never loads its first K tile, so the
+                        // waits on it run out (nothing is left in flight)
+                        const bool withhold = p.test_withhold_k && blockIdx.x == 0 && g == 0;
+                        if (!withhold) {
+                            mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
+                            for (int b = 0; b < D / 64; ++b)
+                                tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
+                                            b * 64, j * kBlockN, bh);
+                        }
                         mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTileBytes);
                         for (int b = 0; b < D / 64; ++b)
                             tma_load_3d(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
@@ -687,7 +696,13 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     }
                 }
                 // LSE = m*alpha + ln(l), natural log of the scaled-score normaliser
-                if (store) p.lse[rowid] = (mc + lg2_approx(l)) * 0.69314718055994531f;
+                if (store) {
+                    const float lse = (mc + lg2_approx(l)) * 0.69314718055994531f;
+                    p.lse[rowid] = lse;
+                    // l = 0 (every Pbar underflowed) or a NaN from 0 * inf in
+                    // a rescale: reported through the status word
+                    if (!isfinite(lse)) atomicOr(p.status, kDevNonFinite);
+                }
             }
             ++ne;
         }
@@ -695,6 +710,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
 
     // O's TMA stores complete before the CTA exits
     if (L::kTmaStoreO && !STATS && warp < kProducerWarp && (threadIdx.x & 127) == 0) bulk_wait0();
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp0) {
@@ -728,16 +744,27 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.scale_log2 = a.scale_log2;
     p.beta = a.beta;
     p.status = a.status;
+    p.test_withhold_k = a.test_withhold_k;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
     p.n_cq = (n_qt + NQ - 1) / NQ;
     p.n_items = a.BH * p.n_cq;
     // persistent: one CTA per SM (or per item, if fewer)
     const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // set-up overlaps the previous kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     prof_begin(STATS ? 1 : 0, stream);
-    kern<<<grid, L::kThreads, L::kAlloc, stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
+    e = cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, p);
     prof_end(STATS ? 1 : 0, stream);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) set_error("fwd launch", e);
     return e;
 }

@@ -26,6 +26,8 @@ struct FwdArgs {
     float beta;         // stabilised-softmax shift factor (mode 1)
     int* status;        // device status word
     int num_sms;        // persistent grid: at most one CTA per SM
+    int test_withhold_k;  // test hook: CTA 0 skips its first K tile load, so
+                          // the waits on it time out (FA_TEST_WITHHOLD_K=1)
 };
 
 struct BwdArgs {
@@ -42,6 +44,8 @@ struct BwdArgs {
     float* dq_acc;                // FP32 [BH, N, d] workspace
     float* lse2;                  // FP32 [BH, Npad] workspace: LSE * log2(e)
     float* delta;                 // FP32 [BH, Npad] workspace: rowsum(dO o O)
+    uint32_t* sync;               // grid barrier words, zero before the first launch
+    int clean;                    // 1: leave dq_acc at zero when done
     void* dq;                     // [BH, N, d] BF16
     void* dk;
     void* dv;

@@ -9,9 +9,10 @@
 
 namespace fa {
 
-// Device status codes written by kernels into the library's status word.
+// Bits that kernels set in the library's device status word.
 constexpr int kDevOk = 0;
-constexpr int kDevTimeout = 5;
+constexpr int kDevTimeout = 1;    // a bounded wait gave up
+constexpr int kDevNonFinite = 2;  // a row's LSE (so its output) is not finite
 
 // A wait gives up after this many nanoseconds of %globaltimer time.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -66,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
     for (uint32_t it = 1;; ++it) {
         if (mbar_test(bar, parity)) return true;
         if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
-            if (status) atomicExch(status, kDevTimeout);
+            if (status) atomicOr(status, kDevTimeout);
             return false;
         }
     }
@@ -127,6 +128,13 @@ __device__ __forceinline__ void bulk_wait_read_le1() {
 }
 
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Every committed bulk group but the N most recent ones has completed (its
+// writes performed, not only its shared-memory source read).
+template <int N>
+__device__ __forceinline__ void bulk_wait_le() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA stores and tcgen05.mma operand reads).
@@ -289,6 +297,83 @@ __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ----------------------------------------------- grid-level synchronisation --
+
+// Programmatic dependent launch: wait until the grids this one depends on in
+// stream order have completed and their memory is visible (a no-op when the
+// launch did not opt in), and let the next grid in the stream begin launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Order this thread's generic-proxy global accesses with async-proxy ones
+// (TMA loads, stores and reductions), in both directions.
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// One thread's part of a barrier over every CTA of the grid, which must all
+// be resident at once (the launch is cooperative).  sync[0] counts arrivals
+// and returns to 0 each time the barrier completes; sync[1] is a generation
+// number that only grows, so the two words stay valid from one launch to the
+// next once zeroed.  The caller first synchronises its CTA (so that this
+// thread's arrival stands for every thread's earlier writes) and afterwards
+// releases the CTA's threads; global writes made before the barrier are then
+// visible after it, to either proxy.  Bounded: a thread that waits longer
+// than kWaitLimitNs records a timeout in *status and returns false.
+__device__ __forceinline__ bool grid_arrive_wait(uint32_t* sync, int* status) {
+    bool ok = true;
+    const uint32_t gen = ld_acquire_gpu(sync + 1);
+    __threadfence();
+    const uint32_t old = atomicAdd(sync, 1u);
+    if (old + 1u == gridDim.x) {
+        atomicExch(sync, 0u);
+        __threadfence();
+        atomicAdd(sync + 1, 1u);
+    } else {
+        const unsigned long long t0 = global_ns();
+        while (ld_acquire_gpu(sync + 1) == gen) {
+            __nanosleep(64);
+            if (global_ns() - t0 > kWaitLimitNs) {
+                if (status) atomicOr(status, kDevTimeout);
+                ok = false;
+                break;
+            }
+        }
+    }
+    __threadfence();
+    fence_async_global();
+    return ok;
+}
+
+// Grid barrier taken by every thread of the CTA (see grid_arrive_wait); the
+// verdict is the same for all of them.
+__device__ __forceinline__ bool grid_barrier(uint32_t* sync, int* status) {
+    fence_async_global();
+    __syncthreads();
+    int ok = 1;
+    if (threadIdx.x == 0) ok = grid_arrive_wait(sync, status) ? 1 : 0;
+    ok = __syncthreads_and(ok);
+    fence_async_global();
+    return ok != 0;
+}
+
+// Named CTA barriers (ids 1..15; id 0 is __syncthreads): `count` threads,
+// a multiple of 32, take part; arrive does not wait.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ math ----
 
 // Packed pairs of FP32 values (one 64-bit register pair) and the paired FP32
@@ -359,6 +444,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a

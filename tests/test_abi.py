@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     names = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_ALLOC", "FA_ERR_CUDA",
-             "FA_ERR_TIMEOUT"]
+             "FA_ERR_TIMEOUT", "FA_ERR_NONFINITE"]
     for code, name in enumerate(names):
         assert fa.fa_status_string(code) == name
     assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"

@@ -32,6 +32,23 @@ def _arrays(c):
     return [f32(getattr(c, n)).reshape(BH, c.N, c.d) for n in ("q", "k", "v", "do")]
 
 
+_EXACT = {}
+
+
+def _exact_bwd(c, key, h=None, rows=None):
+    """The oracle's exact gradients, cached per workload (and head and rows):
+    they do not depend on the mode."""
+    k = (key, h, None if rows is None else rows.tobytes())
+    if k not in _EXACT:
+        qf, kf, vf, gf = _arrays(c)
+        if h is None:
+            _EXACT[k] = orc.bwd(qf, kf, vf, gf, c.causal, c.scale)
+        else:
+            sl = slice(h, h + 1)
+            _EXACT[k] = orc.bwd(qf[sl], kf[sl], vf[sl], gf[sl], c.causal, c.scale, q_rows=rows, k_rows=rows)
+    return _EXACT[k]
+
+
 def _check_full(c, mode, got):
     qf, kf, vf, gf = _arrays(c)
     ex = orc.bwd(qf, kf, vf, gf, c.causal, c.scale)
@@ -59,40 +76,52 @@ def test_shapes_and_tails(fa, d, N, causal):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
-def test_gpt2s_full_size_sampled(fa, mode):
-    c = case("gpt2s")
-    dq, dk, dv = _run(fa, c, mode)
-    qf, kf, vf, gf = _arrays(c)
-    BH = c.B * c.H
-    heads = [0, BH // 2 + mode, BH - 1]
-    rng = np.random.default_rng(100 + mode)
-    for h in heads:
-        sl = slice(h, h + 1)
-        rows = np.unique(np.concatenate([rng.choice(c.N, 96, replace=False), [0, 127, 128, c.N - 1]]))
-        ex = orc.bwd(qf[sl], kf[sl], vf[sl], gf[sl], c.causal, c.scale, q_rows=rows, k_rows=rows)
-        assert rel_fro(dq.reshape(BH, c.N, c.d)[h, rows], ex["dq"]) <= GRAD_REL_TOL
-        assert rel_fro(dk.reshape(BH, c.N, c.d)[h, rows], ex["dk"]) <= GRAD_REL_TOL
-        assert rel_fro(dv.reshape(BH, c.N, c.d)[h, rows], ex["dv"]) <= GRAD_REL_TOL
-
-
-@pytest.mark.parametrize("name,mode", [("gpt2m", 0), ("long", 1), ("ties", 2)])
-def test_other_workloads_full_size_sampled(fa, name, mode):
-    # The remaining workloads at their full sizes (gradients of all heads
-    # computed on the GPU; one head's sampled rows checked against the oracle,
-    # which recomputes that head's LSE and delta itself).
+@pytest.mark.parametrize("name", ["gpt2s", "gpt2m"])
+def test_gpt2_full_size_every_head(fa, name, mode):
+    # Every element of dQ, dK and dV at the GPT-2 shapes, judged per head (a
+    # bad work item cannot hide inside a global norm), in the launch
+    # configuration of the benchmark.
     c = case(name)
-    dq, dk, dv = _run(fa, c, mode)
-    qf, kf, vf, gf = _arrays(c)
+    got = _run(fa, c, mode)
+    ex = _exact_bwd(c, name)
     BH = c.B * c.H
-    h = (BH * 2) // 3
-    rng = np.random.default_rng(200 + mode)
-    rows = np.unique(np.concatenate([rng.choice(c.N, 48, replace=False), [0, 127, 128, c.N - 1]]))
-    sl = slice(h, h + 1)
-    ex = orc.bwd(qf[sl], kf[sl], vf[sl], gf[sl], c.causal, c.scale, q_rows=rows, k_rows=rows)
-    floor = 1e-3 * max(np.linalg.norm(ex[n]) for n in ("dq", "dk", "dv"))
-    assert rel_fro(dq.reshape(BH, c.N, c.d)[h, rows], ex["dq"], floor) <= GRAD_REL_TOL
-    assert rel_fro(dk.reshape(BH, c.N, c.d)[h, rows], ex["dk"], floor) <= GRAD_REL_TOL
-    assert rel_fro(dv.reshape(BH, c.N, c.d)[h, rows], ex["dv"], floor) <= GRAD_REL_TOL
+    for name_g, g in zip(("dq", "dk", "dv"), got):
+        g = g.reshape(BH, c.N, c.d)
+        e = ex[name_g]
+        for h in range(BH):
+            floor = 1e-3 * max(np.linalg.norm(ex[n][h]) for n in ("dq", "dk", "dv"))
+            r = rel_fro(g[h], e[h], floor)
+            assert r <= GRAD_REL_TOL, (name_g, mode, h, r)
+
+
+@pytest.mark.parametrize("name,mode", [("long", 0), ("long", 1), ("long", 2), ("ties", 0), ("ties", 1), ("ties", 2)])
+def test_other_workloads_full_size_sampled(fa, name, mode):
+    # The long-context and tie-stress workloads at full size: sampled query
+    # and key rows of every head against the oracle (which recomputes each
+    # head's LSE and delta itself).  The bound applies to the gradients over
+    # all sampled rows of all heads together (the tensor-level relative
+    # Frobenius error the bound is stated for); each head is also held to 5x
+    # the bound, so that no head can be wrong without failing: on the
+    # tie-stress rows dQ = sum_k dS K_k cancels heavily (duplicated keys,
+    # peaked rows), and 20 rows of one head sit near 1e-2 from BF16 dS alone.
+    c = case(name)
+    got = dict(zip(("dq", "dk", "dv"), (g.reshape(c.B * c.H, c.N, c.d) for g in _run(fa, c, mode))))
+    BH = c.B * c.H
+    rng = np.random.default_rng(200)
+    per_head = 12 if name == "long" else 16
+    diff = {n: 0.0 for n in got}
+    ref = {n: 0.0 for n in got}
+    for h in range(BH):
+        rows = np.unique(np.concatenate([rng.choice(c.N, per_head, replace=False), [0, 127, 128, c.N - 1]]))
+        ex = _exact_bwd(c, name, h, rows)
+        floor = 1e-3 * max(np.linalg.norm(ex[n]) for n in ("dq", "dk", "dv"))
+        for n in got:
+            g = got[n][h, rows]
+            assert rel_fro(g, ex[n], floor) <= 5 * GRAD_REL_TOL, (h, n, rel_fro(g, ex[n], floor))
+            diff[n] += float(np.sum((g - ex[n]) ** 2))
+            ref[n] += float(np.sum(ex[n] ** 2))
+    for n in got:
+        assert np.sqrt(diff[n] / ref[n]) <= GRAD_REL_TOL, (n, np.sqrt(diff[n] / ref[n]))
 
 
 def test_causal_mask_bit_exact_dk_dv(fa):
