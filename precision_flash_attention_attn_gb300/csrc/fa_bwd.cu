@@ -61,7 +61,7 @@ struct BwdParams {
 
 constexpr int kBwdThreads = 512;
 constexpr uint32_t kBarDrained = 1;  // named barrier: the drain warps' reduce-adds have landed (math + drain)
-constexpr uint32_t kBarMath = 2;     // named barrier: the math warps
+constexpr uint32_t kBarGo = 2;       // named barrier: phase C may start (math + drain)
 
 // ------------------------------------------------------------- phase A ----
 // D/8 threads per row, 8 elements (16 bytes of dO) each; each thread takes
@@ -211,8 +211,9 @@ struct BwdLayout {
     static constexpr int kDPEmpty = kDPFull + 1;
     static constexpr int kPFull = kDPEmpty + 1;
     static constexpr int kDSFull = kPFull + 1;
-    static constexpr int kPDSFree = kDSFull + 1;
-    static constexpr int kDQFull = kPDSFree + 1;
+    static constexpr int kPDSFree = kDSFull + 1;     // the tile's dK and dQ products have read dS^T
+    static constexpr int kPtFree = kPDSFree + 1;     // the tile's dV product has read P^T
+    static constexpr int kDQFull = kPtFree + 1;
     static constexpr int kDQEmpty = kDQFull + 1;
     static constexpr int kAccDone = kDQEmpty + 1;    // dK, dV of the item complete
     static constexpr int kAccFree = kAccDone + 1;    // dK, dV read out of TMEM
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         mbar_init(bar(L::kPFull), L::kMathThreads);
         mbar_init(bar(L::kDSFull), L::kMathThreads);
         mbar_init(bar(L::kPDSFree), 1);
+        mbar_init(bar(L::kPtFree), 1);
         mbar_init(bar(L::kDQFull), 1);
         mbar_init(bar(L::kDQEmpty), L::kDrainThreads);
         mbar_init(bar(L::kAccDone), 1);
@@ -479,6 +481,9 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                             mma_bf16_ss(tmem + L::kColDV, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
+                    // P^T may be overwritten once dV has read it, well
+                    // before this tile's dK and dQ are done with dS^T
+                    mma_commit(bar(L::kPtFree));
                 }
                 __syncwarp();
                 if (ahead) {
@@ -633,6 +638,11 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         }
         __syncwarp();
         named_arrive(kBarDrained, L::kMathThreads + L::kDrainThreads);
+        // phase C: these warps convert alongside the math warps
+        named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);
+        fence_async_global();
+        if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
+            convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads + L::kDrainThreads);
     }
     } else {
     regs_inc<L::kRegsMath>();
@@ -699,8 +709,9 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     for (int c = 0; c < 64; ++c)
                         if (c0 + c < kr) pr[c] = 0.f;
                 }
+                // P^T overwrites the previous tile's, which its dV product reads
                 if (g >= 1) {
-                    ok = wait_w(bar(L::kPDSFree), static_cast<uint32_t>(g - 1) & 1u);
+                    ok = wait_w(bar(L::kPtFree), static_cast<uint32_t>(g - 1) & 1u);
                     if (!ok) break;
                 }
                 if (L::kPtInTmem) {
@@ -733,6 +744,8 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 tmem_wait_ld();  // one wait for both loads
                 tc_fence_before();
                 mbar_arrive(bar(L::kDPEmpty));
+                // dS^T into the registers that held P^T, then stored once the
+                // previous tile's dK and dQ products have read dS^T
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -741,27 +754,33 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                         const float4 na = nd4[c / 4];
                         const float4 nb = nd4[c / 4 + 1];
                         const uint32_t* rv = &dpr[h][gq * 8];
-                        float dv8[8];
                         f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[0]), __uint_as_float(rv[1])), alx2,
                                                 f2_pack(na.x, na.y)),
                                          f2_pack(pr[c], pr[c + 1])),
-                                  dv8[0], dv8[1]);
+                                  pr[c], pr[c + 1]);
                         f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[2]), __uint_as_float(rv[3])), alx2,
                                                 f2_pack(na.z, na.w)),
                                          f2_pack(pr[c + 2], pr[c + 3])),
-                                  dv8[2], dv8[3]);
+                                  pr[c + 2], pr[c + 3]);
                         f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[4]), __uint_as_float(rv[5])), alx2,
                                                 f2_pack(nb.x, nb.y)),
                                          f2_pack(pr[c + 4], pr[c + 5])),
-                                  dv8[4], dv8[5]);
+                                  pr[c + 4], pr[c + 5]);
                         f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(rv[6]), __uint_as_float(rv[7])), alx2,
                                                 f2_pack(nb.z, nb.w)),
                                          f2_pack(pr[c + 6], pr[c + 7])),
-                                  dv8[6], dv8[7]);
-                        st_shared_v4(ds_blk + sw128_off(kr, c >> 3), pack_bf16x2(dv8[0], dv8[1]),
-                                     pack_bf16x2(dv8[2], dv8[3]), pack_bf16x2(dv8[4], dv8[5]),
-                                     pack_bf16x2(dv8[6], dv8[7]));
+                                  pr[c + 6], pr[c + 7]);
                     }
+                }
+                if (g >= 1) {
+                    ok = wait_w(bar(L::kPDSFree), static_cast<uint32_t>(g - 1) & 1u);
+                    if (!ok) break;
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int c = ch * 8;
+                    st_shared_v4(ds_blk + sw128_off(kr, ch), pack_bf16x2(pr[c], pr[c + 1]), pack_bf16x2(pr[c + 2], pr[c + 3]),
+                                 pack_bf16x2(pr[c + 4], pr[c + 5]), pack_bf16x2(pr[c + 6], pr[c + 7]));
                 }
                 fence_async_smem();
                 mbar_arrive(bar(L::kDSFull));
@@ -769,19 +788,20 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         }
     }
     // ------------------------------------------------------------ phase C
-    // The math warps convert the dQ accumulator once the drain warps of every
-    // CTA have seen their reduce-adds land.  (Done in this branch, within its
-    // register budget: no register hand-back is needed.)
+    // The math and drain warps (threads 0-383) convert the dQ accumulator
+    // once the drain warps of every CTA have seen their reduce-adds land.
+    // (Each in its own branch, within its register budget: no register
+    // hand-back is needed.)
     named_sync(kBarDrained, L::kMathThreads + L::kDrainThreads);
     if (threadIdx.x == 0) {
         const bool drained = grid_arrive_wait(p.sync, p.status);
         *reinterpret_cast<volatile int*>(smem + L::kFlag) = drained ? 1 : 0;
     }
-    named_sync(kBarMath, L::kMathThreads);
+    named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);
     fence_async_global();
     griddep_launch_dependents();
     if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
-        convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads);
+        convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads + L::kDrainThreads);
     }
     }  // started
 

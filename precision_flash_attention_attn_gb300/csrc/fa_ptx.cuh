@@ -321,33 +321,42 @@ __device__ __forceinline__ void fence_async_global() {
 
 // One thread's part of a barrier over every CTA of the grid, which must all
 // be resident at once (the launch is cooperative).  sync[0] counts arrivals
-// and returns to 0 each time the barrier completes; sync[1] is a generation
-// number that only grows, so the two words stay valid from one launch to the
-// next once zeroed.  The caller first synchronises its CTA (so that this
-// thread's arrival stands for every thread's earlier writes) and afterwards
-// releases the CTA's threads; global writes made before the barrier are then
-// visible after it, to either proxy.  Bounded: a thread that waits longer
-// than kWaitLimitNs records a timeout in *status and returns false.
+// (a reduction without return value, so arriving costs no round trip);
+// thread 0 of CTA 0 waits for the count to reach the grid size, resets it and
+// releases everyone by raising the generation number sync[1], which only
+// grows, so the two words stay valid from one launch to the next once zeroed.
+// The caller first synchronises its CTA (so that this thread's arrival stands
+// for every thread's earlier writes) and afterwards releases the CTA's
+// threads; global writes made before the barrier are then visible after it,
+// to either proxy.  Bounded: a thread that waits longer than kWaitLimitNs
+// records a timeout in *status and returns false.
 __device__ __forceinline__ bool grid_arrive_wait(uint32_t* sync, int* status) {
     bool ok = true;
     const uint32_t gen = ld_acquire_gpu(sync + 1);
     __threadfence();
-    const uint32_t old = atomicAdd(sync, 1u);
-    if (old + 1u == gridDim.x) {
-        atomicExch(sync, 0u);
-        __threadfence();
-        atomicAdd(sync + 1, 1u);
-    } else {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire_gpu(sync + 1) == gen) {
-            __nanosleep(64);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sync) : "memory");
+    const unsigned long long t0 = global_ns();
+    if (blockIdx.x == 0) {
+        while (ld_acquire_gpu(sync) != gridDim.x) {
             if (global_ns() - t0 > kWaitLimitNs) {
-                if (status) atomicOr(status, kDevTimeout);
+                ok = false;
+                break;
+            }
+        }
+        if (ok) {
+            atomicExch(sync, 0u);
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(sync + 1), "r"(gen + 1u) : "memory");
+        }
+    } else {
+        while (ld_acquire_gpu(sync + 1) == gen) {
+            if (global_ns() - t0 > kWaitLimitNs) {
                 ok = false;
                 break;
             }
         }
     }
+    if (!ok && status) atomicOr(status, kDevTimeout);
     __threadfence();
     fence_async_global();
     return ok;
