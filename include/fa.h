@@ -95,11 +95,18 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *          (exp(-(beta-1)*scale*rm) below the FP32 range), and O then is not
  *          finite; the section restricts the rule to rows where the plain
  *          softmax is stable.
- *   eps  : the tolerance of the tie test rm - S <= eps.  Only eps = 0, exact
- *          ties of the FP32 raw scores, is supported (FA_ERR_UNSUPPORTED
- *          otherwise): in a single tiled pass a key counted within eps of a
- *          running maximum may fall out of range when a later tile raises the
- *          maximum, so eps > 0 needs the whole row first.
+ *   eps  : the tolerance of the tie test, in scaled units: rs counts the keys
+ *          with scale*(rm - q.k) <= eps.  eps = 0 counts exact ties of the
+ *          FP32 raw scores, tracked through the tiled forward with a running
+ *          maximum and count.  eps > 0 (the section uses about 1e-3): a key
+ *          counted within eps of a running maximum can drop out of range when
+ *          a later key tile raises the maximum, so the whole row is needed
+ *          first.  A pre-pass on CUDA cores (FP32 scores, one fixed summation
+ *          order) finds each row's rm, rs and shift; the tensor-core forward
+ *          then uses that shift from its first key tile on.  Costs a
+ *          stream-ordered workspace of B*H*N*4 bytes (fa_fwd_ex) or B*H*N*8
+ *          bytes (fa_tie_stats_ex), cudaMallocAsync on `stream` (FA_ERR_ALLOC
+ *          if that fails), and two extra passes of QK^T on CUDA cores.
  * A NULL pointer selects the defaults (beta = FA_STAB_BETA_DEFAULT, eps = 0).
  * Modes 0 and 2 check the parameters but do not use them.
  */
@@ -112,7 +119,7 @@ typedef struct {
 /*
  * fa_fwd_ex -- fa_fwd with explicit stabilised-softmax parameters.
  * FA_ERR_INVALID_ARG if beta is not a finite value > 1 or eps is negative or
- * not finite; FA_ERR_UNSUPPORTED if eps > 0.  Otherwise as fa_fwd.
+ * not finite.  Otherwise as fa_fwd (plus the eps > 0 pre-pass in mode 1).
  */
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
               int B, int H, int N, int d, int causal, float scale, int mode,
@@ -154,13 +161,23 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
  *                              (cudaMallocAsync on `stream`, on top of
  *                              fa_bwd's), and delta is formed from it; o is
  *                              not read and may be NULL.
- * P is recomputed from the caller's lse either way, so only delta's source
+ *   FA_DELTA_FROM_DP_P         delta = rowsum(dP o P) (section 3.4.2, "Failure
+ *                              is linked to the computation of delta"; the
+ *                              delta substitution of section 5): equal to
+ *                              rowsum(dO o O) in exact arithmetic, formed
+ *                              without any output.  A pre-pass on CUDA cores
+ *                              recomputes P = exp(scale*q.k - lse) and
+ *                              dP = dO.v in FP32 over each row (compensated
+ *                              sum) into fa_bwd's workspace; o is not read
+ *                              and may be NULL, `mode` is only checked.
+ * P is recomputed from the caller's lse in every case, so only delta's source
  * changes.  Other arguments and errors as fa_bwd; FA_ERR_INVALID_ARG for an
  * unknown delta_source.
  */
 typedef enum {
     FA_DELTA_STORED_O = 0,
-    FA_DELTA_RECOMPUTED_O_FP32 = 1
+    FA_DELTA_RECOMPUTED_O_FP32 = 1,
+    FA_DELTA_FROM_DP_P = 2
 } fa_delta_source_t;
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dO, void* dq, void* dk, void* dv,
@@ -234,8 +251,9 @@ int fa_tie_stats(const void* q, const void* k, const void* v, const void* o,
  *               delta_hp)[T]"), O_ref standing in for the FP32 output O_hp;
  *   dO        : BF16 [B, H, N, d], read only when delta_err is set (then
  *               both must be 16-byte aligned device pointers).
- * The p_one counts of mode 1 follow beta; o must come from fa_fwd_ex with the
- * same parameters.
+ * The p_one counts of mode 1 follow beta and eps; o must come from fa_fwd_ex
+ * with the same parameters.  With eps > 0, tie_count[r] is the row's
+ * near-tie count rs (every mode), from the row pre-pass.
  */
 int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o,
                     int B, int H, int N, int d, int causal, float scale, int mode,

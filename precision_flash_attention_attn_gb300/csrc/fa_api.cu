@@ -122,16 +122,35 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
 }
 
 // Stabilised-softmax parameters (NULL: the defaults).  "The modified safe
-// softmax" of section 3.4.5 requires beta > 1; only exact ties (eps = 0) are
-// supported by the one-pass tiled forward.
-int check_params(const fa_stab_params_t* prm, float* beta) {
+// softmax" of section 3.4.5 requires beta > 1 and a tolerance eps >= 0.
+int check_params(const fa_stab_params_t* prm, float* beta, float* eps) {
     *beta = FA_STAB_BETA_DEFAULT;
+    *eps = 0.f;
     if (!prm) return FA_OK;
     if (!std::isfinite(prm->beta) || !(prm->beta > 1.f)) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(prm->eps) || prm->eps < 0.f) return FA_ERR_INVALID_ARG;
-    if (prm->eps != 0.f) return FA_ERR_UNSUPPORTED;
     *beta = prm->beta;
+    *eps = prm->eps;
     return FA_OK;
+}
+
+// Enqueue the row pre-pass (row maximum, near-tie count, shift).
+int launch_row_pass(const void* q, const void* k, int BH, int N, int d, int causal, float scale, int mode,
+                    float beta, float eps, float* shift, int32_t* rs, cudaStream_t st) {
+    fa::RowShiftArgs r{};
+    r.q = q;
+    r.k = k;
+    r.shift = shift;
+    r.rs = rs;
+    r.BH = BH;
+    r.N = N;
+    r.d = d;
+    r.causal = causal;
+    r.mode = mode;
+    r.scale = scale;
+    r.beta = beta;
+    r.eps = eps;
+    return fa::launch_row_shift(r, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
@@ -170,7 +189,7 @@ bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o,
 // zero region at zero again.  Arguments are already validated.
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
-                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st) {
+                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0) {
     const int BH = B * H;
     const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
     char* zb = static_cast<char*>(zero);
@@ -203,6 +222,7 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     a.delta = delta;
     a.sync = sync;
     a.clean = clean;
+    a.delta_given = delta_given;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -286,8 +306,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
-    float beta = 0.f;
-    if ((rc = check_params(params, &beta))) return rc;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
@@ -319,7 +339,24 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.num_sms = di->num_sms;
     const char* hook = std::getenv("FA_TEST_WITHHOLD_K");
     a.test_withhold_k = (hook && hook[0] == '1') ? 1 : 0;
-    return fa::launch_fwd(a, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mode != FA_MODE_STABILISED || eps == 0.f)
+        return fa::launch_fwd(a, false, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    // A tolerance: each row's shift from a pre-pass over the whole row, held
+    // fixed through the tiled forward (stream-ordered workspace, B*H*N*4 bytes).
+    void* ws = nullptr;
+    cudaError_t ae = cudaMallocAsync(&ws, static_cast<size_t>(BH) * N * sizeof(float), st);
+    if (ae != cudaSuccess || !ws) {
+        fa::set_error("cudaMallocAsync(row shifts)", ae);
+        cudaGetLastError();
+        return FA_ERR_ALLOC;
+    }
+    a.shift = static_cast<float*>(ws);
+    rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, static_cast<float*>(ws), nullptr, st);
+    if (rc == FA_OK && fa::launch_fwd(a, false, st) != cudaSuccess) rc = FA_ERR_CUDA;
+    const cudaError_t fe = cudaFreeAsync(ws, st);
+    if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(row shifts)", fe);
+    return rc;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
@@ -365,7 +402,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               int delta_source, fa_stream_t stream) {
     if (delta_source == FA_DELTA_STORED_O)
         return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, stream);
-    if (delta_source != FA_DELTA_RECOMPUTED_O_FP32) return FA_ERR_INVALID_ARG;
+    if (delta_source != FA_DELTA_RECOMPUTED_O_FP32 && delta_source != FA_DELTA_FROM_DP_P) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv))
         return FA_ERR_INVALID_ARG;
@@ -373,12 +410,52 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     if (rc) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
-    const size_t o_bytes = static_cast<size_t>(B) * H * N * d * sizeof(float);  // a multiple of 256
-    const size_t lse_bytes = static_cast<size_t>(B) * H * N * sizeof(float);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    void* ws = nullptr;
     const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
     if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    if (delta_source == FA_DELTA_FROM_DP_P) {
+        // delta = rowsum(dP o P) from a pre-pass into the backward's row
+        // workspace; the stored o is not read
+        const int BH = B * H;
+        const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
+        const BwdSizes z = bwd_sizes(BH, N, d);
+        reserve_pool(di, z.zero_bytes() + z.row_bytes());
+        void* ws = nullptr;
+        cudaError_t ae = cudaMallocAsync(&ws, z.zero_bytes() + z.row_bytes(), st);
+        if (ae != cudaSuccess || !ws) {
+            fa::set_error("cudaMallocAsync(workspace)", ae);
+            cudaGetLastError();
+            return FA_ERR_ALLOC;
+        }
+        cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
+        if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
+        float* rows = reinterpret_cast<float*>(static_cast<char*>(ws) + z.zero_bytes());
+        if (rc == FA_OK) {
+            fa::DeltaPdpArgs pa{};
+            pa.q = q;
+            pa.k = k;
+            pa.v = v;
+            pa.dout = dO;
+            pa.lse = lse;
+            pa.delta = rows + static_cast<size_t>(BH) * Npad;
+            pa.BH = BH;
+            pa.N = N;
+            pa.Npad = Npad;
+            pa.d = d;
+            pa.causal = causal;
+            pa.scale = scale;
+            if (fa::launch_delta_pdp(pa, st) != cudaSuccess) rc = FA_ERR_CUDA;
+        }
+        // o is not read: delta is given; pass a valid pointer for the unused argument
+        if (rc == FA_OK)
+            rc = launch_backward(q, k, v, dO, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, 0, di, ws, rows, 0, st, 1);
+        const cudaError_t fe = cudaFreeAsync(ws, st);
+        if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
+        return rc;
+    }
+    const size_t o_bytes = static_cast<size_t>(B) * H * N * d * sizeof(float);  // a multiple of 256
+    const size_t lse_bytes = static_cast<size_t>(B) * H * N * sizeof(float);
+    void* ws = nullptr;
     cudaError_t ae = cudaMallocAsync(&ws, o_bytes + lse_bytes, st);
     if (ae != cudaSuccess || !ws) {
         fa::set_error("cudaMallocAsync(recomputed O)", ae);
@@ -487,8 +564,8 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
         return FA_ERR_INVALID_ARG;
     int rc = check_common(B, H, N, d, causal, scale, mode);
     if (rc) return rc;
-    float beta = 0.f;
-    if ((rc = check_params(params, &beta))) return rc;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
     DeviceInfo* di = nullptr;
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
@@ -517,7 +594,29 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
     a.scale_log2 = log2e_times(scale);
     a.status = di->status;
     a.num_sms = di->num_sms;
-    if (fa::launch_fwd(a, true, st) != cudaSuccess) return FA_ERR_CUDA;
+    // A tolerance: the near-tie counts (and, in mode 1, each row's fixed
+    // shift) from the row pre-pass (stream-ordered workspace, B*H*N*8 bytes).
+    void* ws = nullptr;
+    if (eps != 0.f) {
+        const size_t nrow = static_cast<size_t>(BH) * N;
+        cudaError_t ae = cudaMallocAsync(&ws, nrow * (sizeof(float) + sizeof(int32_t)), st);
+        if (ae != cudaSuccess || !ws) {
+            fa::set_error("cudaMallocAsync(row statistics)", ae);
+            cudaGetLastError();
+            return FA_ERR_ALLOC;
+        }
+        float* shift = static_cast<float*>(ws);
+        int32_t* rs = reinterpret_cast<int32_t*>(shift + nrow);
+        if (mode == FA_MODE_STABILISED) a.shift = shift;
+        a.rs_in = rs;
+        rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, shift, rs, st);
+    }
+    if (rc == FA_OK && fa::launch_fwd(a, true, st) != cudaSuccess) rc = FA_ERR_CUDA;
+    if (ws) {
+        const cudaError_t fe = cudaFreeAsync(ws, st);
+        if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(row statistics)", fe);
+    }
+    if (rc != FA_OK) return rc;
     fa::StatsArgs s{};
     s.q = q;
     s.k = k;

@@ -52,6 +52,7 @@ struct BwdParams {
     float* delta;         // [BH, Npad]: -alpha*rowsum(dO o O), 0 on padded rows
     uint32_t* sync;       // grid barrier words (zero before the first launch)
     int clean;            // 1: leave the accumulator and the barrier words at zero afterwards
+    int delta_given;      // 1: delta already holds -alpha*rowsum(dP o P); phase A forms lse2 only
     int BH, N, Npad, mode;
     int n_kt;     // key tiles per (batch, head)
     int n_items;  // BH * n_kt
@@ -91,7 +92,9 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p) {
             valid[u] = r < rows && i < p.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
             lse[u] = 0.f;
-            if (valid[u]) {
+            if (valid[u] && p.delta_given) {
+                if (sub == 0) lse[u] = p.lse[static_cast<size_t>(bh) * p.N + i];
+            } else if (valid[u]) {
                 const size_t row = static_cast<size_t>(bh) * p.N + i;
                 const size_t base = row * D + sub * 8;
                 g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
@@ -130,7 +133,7 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p) {
                 // stored pre-negated / pre-scaled for the main phase's FMAs:
                 //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
                 //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
-                p.delta[r] = valid[u] ? -p.scale * acc : 0.f;
+                if (!p.delta_given) p.delta[r] = valid[u] ? -p.scale * acc : 0.f;
                 // padded rows: P = exp2(s - inf) = 0
                 p.lse2[r] = valid[u] ? -lse[u] * log2e : -INFINITY;
             }
@@ -833,6 +836,7 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.delta = a.delta;
     p.sync = a.sync;
     p.clean = a.clean;
+    p.delta_given = a.delta_given;
     p.mode = a.mode;
     p.BH = a.BH;
     p.N = a.N;

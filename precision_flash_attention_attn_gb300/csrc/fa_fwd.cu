@@ -116,6 +116,8 @@ struct FwdParams {
     float beta;   // mode 1: shift factor of rows with a positive repeated maximum
     int* status;
     int test_withhold_k;  // test hook (see FwdArgs)
+    const float* shift;   // mode 1, nullable: fixed per-row shift (see FwdArgs)
+    const int32_t* rs_in; // statistics variant, nullable: tie counts to report
 };
 
 // Work items are (query-tile group, batch-head) pairs, numbered longest first
@@ -417,6 +419,9 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
             float mc = -INFINITY; // m * sl2
             float l = 0.f;
             int ones0 = 0, ones1 = 0;
+            // mode 1 with a tolerance: the row's shift, found by a pre-pass
+            // over the whole row, holds from the first key tile on
+            const float m_fix = (MODE == 1 && p.shift && qrow < p.N) ? p.shift[static_cast<size_t>(bh) * p.N + qrow] : 0.f;
             for (int j = 0; j < nkt; ++j, ++cs) {
                 ok = wait_w(bar(L::kSFull + t), static_cast<uint32_t>(cs) & 1u);
                 if (!ok) break;
@@ -517,7 +522,9 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     M = fmaxf(M, tm);
                 }
                 float m_new = M;
-                if (MODE == 1 && C > 1) {
+                if (MODE == 1 && p.shift) {
+                    m_new = m_fix;
+                } else if (MODE == 1 && C > 1) {
                     if (M > 0.f) m_new = p.beta * M;
                     else if (M < 0.f) m_new = 0.f;
                 }
@@ -620,7 +627,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(bar(L::kOFree + t));
                 if (store) {
-                    p.tie_count[rowid] = C;
+                    p.tie_count[rowid] = p.rs_in ? p.rs_in[rowid] : C;
                     if (p.p_one) {
                         p.p_one[rowid] = ones0;
                         p.p_one[static_cast<size_t>(p.BH) * p.N + rowid] = ones1;
@@ -745,6 +752,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.beta = a.beta;
     p.status = a.status;
     p.test_withhold_k = a.test_withhold_k;
+    p.shift = a.shift;
+    p.rs_in = a.rs_in;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
     p.n_cq = (n_qt + NQ - 1) / NQ;
     p.n_items = a.BH * p.n_cq;

@@ -28,7 +28,37 @@ struct FwdArgs {
     int num_sms;        // persistent grid: at most one CTA per SM
     int test_withhold_k;  // test hook: CTA 0 skips its first K tile load, so
                           // the waits on it time out (FA_TEST_WITHHOLD_K=1)
+    const float* shift;   // nullable, mode 1: fixed per-row shift [BH, N] (raw
+                          // score units) used from the first key tile on
+    const int32_t* rs_in; // nullable, statistics variant: tie counts to report
 };
+
+// Row statistics pre-pass of the stabilised softmax with a tolerance eps:
+// per row the maximum rm of the raw scores, rs = #{j: scale*(rm - s_j) <= eps}
+// and the mode's shift m(rm, rs).
+struct RowShiftArgs {
+    const void* q;
+    const void* k;
+    float* shift;   // nullable: [BH, N] shift, raw score units
+    int32_t* rs;    // nullable: [BH, N] near-tie counts
+    int BH, N, d, causal, mode;
+    float scale, beta, eps;
+};
+cudaError_t launch_row_shift(const RowShiftArgs& a, cudaStream_t stream);
+
+// delta = rowsum(dP o P) pre-pass of the backward (written as -scale*delta
+// into the padded row array [BH, Npad]).
+struct DeltaPdpArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dout;
+    const float* lse;  // [BH, N]
+    float* delta;      // [BH, Npad]
+    int BH, N, Npad, d, causal;
+    float scale;
+};
+cudaError_t launch_delta_pdp(const DeltaPdpArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
     const CUtensorMap* tm_q;
@@ -46,6 +76,7 @@ struct BwdArgs {
     float* delta;                 // FP32 [BH, Npad] workspace: rowsum(dO o O)
     uint32_t* sync;               // grid barrier words, zero before the first launch
     int clean;                    // 1: leave dq_acc at zero when done
+    int delta_given;              // 1: delta is already in place (rowsum(dP o P) pre-pass)
     void* dq;                     // [BH, N, d] BF16
     void* dk;
     void* dv;

@@ -47,6 +47,7 @@ _lib.fa_fwd_ex.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, 
 _lib.fa_bwd_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _i, _P]
 DELTA_STORED_O = 0            # delta from the caller's o (fa_bwd)
 DELTA_RECOMPUTED_O_FP32 = 1   # delta from O recomputed as P V in FP32 inside the backward
+DELTA_FROM_DP_P = 2           # delta = rowsum(dP o P), no output read
 _lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []

@@ -115,11 +115,10 @@ def _stats_ex(beta, eps, **kw):
     return fa.fa_tie_stats_ex(**a)
 
 
-# "The modified safe softmax" requires beta > 1; only exact ties (eps = 0) are
-# supported, any other finite eps >= 0 is FA_ERR_UNSUPPORTED (2)
+# "The modified safe softmax" requires beta > 1 and a tolerance eps >= 0
 BAD_PARAMS = [
     (1.0, 0.0, 1), (0.5, 0.0, 1), (-2.0, 0.0, 1), (float("nan"), 0.0, 1), (float("inf"), 0.0, 1),
-    (2.0, -1e-3, 1), (2.0, float("nan"), 1), (2.0, float("inf"), 1), (2.0, 1e-3, 2), (8.0, 1.0, 2),
+    (2.0, -1e-3, 1), (2.0, float("nan"), 1), (2.0, float("inf"), 1),
 ]
 
 
@@ -128,6 +127,15 @@ def test_stab_params_rejected(beta, eps, code):
     for mode in (0, 1, 2):  # checked in every mode, used only in mode 1
         assert _fwd_ex(beta, eps, mode=mode) == code
         assert _stats_ex(beta, eps, mode=mode) == code
+
+
+@pytest.mark.parametrize("beta,eps", [(2.0, 1e-3), (8.0, 1.0), (4.0, 0.0)])
+def test_valid_stab_params_pass_validation(beta, eps):
+    # accepted parameters get past argument checking: without a GPU the call
+    # then fails on the device, never with FA_ERR_INVALID_ARG / UNSUPPORTED
+    for mode in (0, 1, 2):
+        assert _fwd_ex(beta, eps, mode=mode) not in (0, 1, 2)
+        assert _stats_ex(beta, eps, mode=mode) not in (0, 1, 2)
 
 
 def test_argument_errors_precede_parameter_errors():
@@ -150,12 +158,12 @@ def _bwd_ex(source, **kw):
     return fa.fa_bwd_ex(**a)
 
 
-@pytest.mark.parametrize("source", [2, -1, 100])
+@pytest.mark.parametrize("source", [3, -1, 100])
 def test_bwd_ex_unknown_delta_source(source):
     assert _bwd_ex(source) == 1
 
 
-@pytest.mark.parametrize("source", [0, 1])
+@pytest.mark.parametrize("source", [0, 1, 2])
 @pytest.mark.parametrize("kw", [dict(q=0), dict(dO=0), dict(dq=MISALIGNED), dict(lse=0), dict(N=0), dict(mode=3)])
 def test_bwd_ex_invalid_arguments(source, kw):
     assert _bwd_ex(source, **kw) == 1

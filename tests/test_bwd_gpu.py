@@ -171,3 +171,44 @@ def test_delta_from_recomputed_fp32_output(fa, mode):
     assert (got[0].float() - ref[0].float()).abs().max().item() <= 1e-2 * ref[0].float().abs().max().item()
     stored = fa.attention_bwd(q, k, v, o, lse, do, c.causal, c.scale, mode)
     assert not torch.equal(stored[1], got[1])  # delta's source matters
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_delta_from_dp_p(fa, mode):
+    # The delta substitution of section 5: delta = rowsum(dP o P), equal to
+    # rowsum(dO o O) in exact arithmetic, formed without the stored output.
+    # Gradients stay within the oracle's bound; dQ and dK (the gradients that
+    # delta enters) land next to those of the FP32-output delta (both
+    # approximate the exact delta to FP32 rounding) and apart from the
+    # stored-BF16-O ones; dV = P^T dO does not involve delta and is
+    # bit-identical across the three.
+    import torch
+    c = case("tiny")
+    q, k, v, do = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
+    got = fa.attention_bwd(q, k, v, None, lse, do, c.causal, c.scale, mode, delta_source=fa.DELTA_FROM_DP_P)
+    assert fa.fa_device_status() == 0
+    _check_full(c, mode, [host_f64(t) for t in got])
+    o32 = fa.attention_bwd(q, k, v, None, lse, do, c.causal, c.scale, mode, delta_source=fa.DELTA_RECOMPUTED_O_FP32)
+    stored = fa.attention_bwd(q, k, v, o, lse, do, c.causal, c.scale, mode)
+    torch.cuda.synchronize()
+    for i in (0, 1):  # dQ, dK
+        near = (got[i].float() - o32[i].float()).norm().item()
+        far = (stored[i].float() - o32[i].float()).norm().item()
+        assert near < far, (i, near, far)
+    assert torch.equal(got[2], o32[2]) and torch.equal(got[2], stored[2])
+
+
+def test_delta_from_dp_p_gpt2s_sampled(fa):
+    c = case("gpt2s")
+    q, k, v, do = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, 1)
+    got = fa.attention_bwd(q, k, v, None, lse, do, c.causal, c.scale, 1, delta_source=fa.DELTA_FROM_DP_P)
+    assert fa.fa_device_status() == 0
+    BH = c.B * c.H
+    rng = np.random.default_rng(300)
+    for h in (0, BH // 2, BH - 1):
+        rows = np.unique(np.concatenate([rng.choice(c.N, 48, replace=False), [0, 127, 128, c.N - 1]]))
+        ex = _exact_bwd(c, "gpt2s", h, rows)
+        for n, g in zip(("dq", "dk", "dv"), got):
+            assert rel_fro(host_f64(g).reshape(BH, c.N, c.d)[h, rows], ex[n]) <= GRAD_REL_TOL, (h, n)
