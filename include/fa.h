@@ -263,6 +263,30 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o,
                     fa_stream_t stream);
 
 /*
+ * fa_delta_error_split -- the decomposition of delta_lp - delta_hp for a
+ * stored output o of `mode` (section 3.4.4, "Cause 2: Biased Rounding Error
+ * Leads to Positive (delta_lp - delta_hp)[T]"; the quantitative decomposition
+ * the page lists among the missing experiments).  Per row r, with the row's
+ * shift m (the untiled rule of the mode with the parameters' beta and eps),
+ * P_j = exp(scale*q.k_j - m), b_j = bf16(P_j), l = sum_j P_j and the FP32
+ * reference probabilities p_j (exact row maximum, compensated sums):
+ *   err_one[r]  = sum_c dO[r,c] sum_{j: b_j = 1}  (b_j / l - p_j) v_j[c]
+ *   err_rest[r] = sum_c dO[r,c] sum_{j: b_j != 1} (b_j / l - p_j) v_j[c]
+ *   err_out[r]  = sum_c dO[r,c] (o[r,c] - sum_j b_j v_j[c] / l)
+ * so that err_one + err_rest + err_out = sum_c dO (o - O_ref), the delta_err
+ * of fa_tie_stats_ex.  The split follows the untiled softmax (a key's
+ * probability with the row's final shift); in the tiled forward a running
+ * maximum may have been fed as 1 and rescaled later.  q, k, v, dO BF16
+ * [B,H,N,d]; o BF16 (FP32 in mode 2); outputs FP32 [B,H,N].  Diagnostic: CUDA
+ * cores, FP32, about (d/8 + 3) passes over each row's keys.
+ */
+int fa_delta_error_split(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, int B, int H, int N, int d, int causal,
+                         float scale, int mode, const fa_stab_params_t* params,
+                         float* err_one, float* err_rest, float* err_out,
+                         fa_stream_t stream);
+
+/*
  * fa_device_status -- synchronises `stream`, then returns FA_ERR_TIMEOUT if any
  * kernel of this library on the current device recorded a bounded-wait
  * timeout since the last reset, else FA_ERR_NONFINITE if a forward wrote a

@@ -63,6 +63,8 @@ static double score(const float* q, const float* k, int d) {
 
 static int n_visible(int i, int N, int causal) { return causal ? i + 1 : N; }
 
+static float bf16_round(float x);  /* round to nearest even BF16 (defined below) */
+
 /* Shift for one row in scaled units (section 3.4.5).  rmz = alpha * rowmax,
  * rs = number of keys at the maximum. */
 static double row_shift(double rmz, long rs, int mode, double beta) {
@@ -138,6 +140,89 @@ int oracle_fwd(const float* q, const float* k, const float* v, const float* dout
             }
         }
         free(s);
+    }
+    return err;
+}
+
+/* ---- decomposition of the delta error --------------------------------------
+ * For a stored output o of a mode, split delta_lp - delta_hp = sum_c dO[c] *
+ * (o[c] - O_hp[c]) (section 3.4.4, "Cause 2: Biased Rounding Error Leads to
+ * Positive (delta_lp - delta_hp)[T]") into the quantitative decomposition the
+ * page lists as missing: the keys whose BF16 probability is exactly 1, the
+ * other keys, and the rounding of the output itself.  With the row's shift m
+ * (the untiled rule of the mode with tolerance eps, scaled units),
+ *   P_j = fp32(exp(alpha s_j - m)),  b_j = bf16(P_j),  l = sum_j P_j,
+ *   p_j = exp(alpha s_j - LSE)        (exact probabilities, O_hp = sum p_j v_j)
+ *   one  = sum_c dO[c] sum_{j: b_j = 1}  (b_j / l - p_j) v_j[c]
+ *   rest = sum_c dO[c] sum_{j: b_j != 1} (b_j / l - p_j) v_j[c]
+ *   out  = sum_c dO[c] (o[c] - sum_j b_j v_j[c] / l)
+ * so that one + rest + out = sum_c dO[c] (o[c] - O_hp[c]). */
+int oracle_delta_split(const float* q, const float* k, const float* v, const float* o,
+                       const float* dout, int64_t BH, int N, int d, int causal, double alpha,
+                       int mode, double beta, double eps, const int64_t* rows, int64_t nrows,
+                       double* one, double* rest, double* out) {
+    if (!rows) nrows = BH * (int64_t)N;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* acc = (double*)malloc(sizeof(double) * 5 * (size_t)d);
+        if (!s || !acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (!s || !acc) continue;
+            int64_t flat = rows ? rows[r] : r;
+            int64_t bh = flat / N;
+            int i = (int)(flat % N);
+            const size_t off = (size_t)bh * N * d;
+            const float* qi = q + off + (size_t)i * d;
+            int nv = n_visible(i, N, causal);
+            double rm = -INFINITY;
+            for (int j = 0; j < nv; ++j) {
+                s[j] = score(qi, k + off + (size_t)j * d, d);
+                if (s[j] > rm) rm = s[j];
+            }
+            long rs = 0;
+            for (int j = 0; j < nv; ++j) rs += (eps == 0.0) ? (s[j] == rm) : (alpha * (rm - s[j]) <= eps);
+            double m = row_shift(alpha * rm, rs, mode, beta);
+            double lref = 0.0, l = 0.0;
+            for (int j = 0; j < nv; ++j) {
+                lref += exp(alpha * (s[j] - rm));
+                l += (double)(float)exp(alpha * s[j] - m);
+            }
+            /* acc: [0] sum_{b=1} b v, [1] sum_{b=1} p v, [2] sum_{b!=1} b v, [3] sum_{b!=1} p v */
+            for (int c = 0; c < 4 * d; ++c) acc[c] = 0.0;
+            for (int j = 0; j < nv; ++j) {
+                float pj32 = (float)exp(alpha * s[j] - m);
+                double b = (double)bf16_round(pj32);
+                double pr = exp(alpha * (s[j] - rm)) / lref;
+                const float* vj = v + off + (size_t)j * d;
+                int base = (b == 1.0) ? 0 : 2;
+                for (int c = 0; c < d; ++c) {
+                    acc[(size_t)base * d + c] += b * (double)vj[c];
+                    acc[(size_t)(base + 1) * d + c] += pr * (double)vj[c];
+                }
+            }
+            const float* g = dout + off + (size_t)i * d;
+            const float* oi = o + off + (size_t)i * d;
+            double e1 = 0.0, e2 = 0.0, e3 = 0.0;
+            for (int c = 0; c < d; ++c) {
+                double one_c = acc[c] / l - acc[(size_t)d + c];
+                double rest_c = acc[(size_t)2 * d + c] / l - acc[(size_t)3 * d + c];
+                double lp_c = (acc[c] + acc[(size_t)2 * d + c]) / l;
+                e1 += (double)g[c] * one_c;
+                e2 += (double)g[c] * rest_c;
+                e3 += (double)g[c] * ((double)oi[c] - lp_c);
+            }
+            one[r] = e1;
+            rest[r] = e2;
+            out[r] = e3;
+        }
+        free(s);
+        free(acc);
     }
     return err;
 }

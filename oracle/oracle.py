@@ -51,6 +51,9 @@ def lib():
         L.oracle_bf16_round.argtypes = [P, P, i64]
         L.oracle_fwd_emul.argtypes = [P, P, P, i64, i32, i32, i32, f64, i32, f64, i32, P, i64,
                                       P, P, P, P, P, P, P]
+        L.oracle_delta_split.argtypes = [P, P, P, P, P, i64, i32, i32, i32, f64, i32, f64, f64, P, i64,
+                                         P, P, P]
+        L.oracle_delta_split.restype = ctypes.c_int
         L.oracle_row_shift.argtypes = [f64, ctypes.c_long, i32, f64]
         L.oracle_row_shift.restype = f64
         for f in (L.oracle_fwd, L.oracle_bwd_dq, L.oracle_bwd_dkdv, L.oracle_fwd_emul,
@@ -179,3 +182,24 @@ def fwd_emul(q, k, v, causal, scale, mode=0, beta=BETA, block_n=128, rows=None):
         out = {kk: (vv.reshape(BH, N, d) if vv.ndim == 2 else vv.reshape(BH, N))
                for kk, vv in out.items()}
     return out
+
+
+def delta_split(q, k, v, o, dout, causal, scale, mode=0, beta=BETA, eps=0.0, rows=None):
+    """Decomposition of sum_c dO (o - O_hp) per row (see attn_ref.c):
+    returns dict(one, rest, out) -- the keys whose BF16 probability is 1, the
+    other keys, and the output rounding.  o is a stored output [BH, N, d]
+    (float32 values), dout the loss gradient."""
+    q, k, v, o, g = _f32(q), _f32(k), _f32(v), _f32(o), _f32(dout)
+    BH, N, d = q.shape
+    r, nr = _rows(rows)
+    n = BH * N if r is None else nr
+    one, rest, out = (np.empty(n, np.float64) for _ in range(3))
+    rc = lib().oracle_delta_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(g), BH, N, d, int(causal),
+                                  float(scale), int(mode), float(beta), float(eps), _ptr(r), nr,
+                                  _ptr(one), _ptr(rest), _ptr(out))
+    if rc:
+        raise MemoryError("oracle_delta_split failed")
+    res = {"one": one, "rest": rest, "out": out}
+    if r is None:
+        res = {kk: vv.reshape(BH, N) for kk, vv in res.items()}
+    return res

@@ -635,6 +635,38 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
     return fa::launch_pv_err(s, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa_delta_error_split(const void* q, const void* k, const void* v, const void* o, const void* dO, int B, int H,
+                         int N, int d, int causal, float scale, int mode, const fa_stab_params_t* params,
+                         float* err_one, float* err_rest, float* err_out, fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+        !aligned16(err_one) || !aligned16(err_rest) || !aligned16(err_out))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    fa::SplitArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dO;
+    a.err_one = err_one;
+    a.err_rest = err_rest;
+    a.err_out = err_out;
+    a.BH = B * H;
+    a.N = N;
+    a.d = d;
+    a.causal = causal;
+    a.mode = mode;
+    a.scale = scale;
+    a.beta = beta;
+    a.eps = eps;
+    return fa::launch_delta_split(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_device_status(fa_stream_t stream, int reset) {
     DeviceInfo* di = nullptr;
     int rc = device_info(&di);

@@ -21,4 +21,19 @@ struct StatsArgs {
 
 cudaError_t launch_pv_err(const StatsArgs& a, cudaStream_t stream);
 
+struct SplitArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;     // BF16 or FP32 (mode 2)
+    const void* dout;  // BF16
+    float* err_one;    // [BH, N] each
+    float* err_rest;
+    float* err_out;
+    int BH, N, d, causal, mode;
+    float scale, beta, eps;
+};
+
+cudaError_t launch_delta_split(const SplitArgs& a, cudaStream_t stream);
+
 }  // namespace fa

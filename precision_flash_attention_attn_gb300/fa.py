@@ -49,6 +49,7 @@ DELTA_STORED_O = 0            # delta from the caller's o (fa_bwd)
 DELTA_RECOMPUTED_O_FP32 = 1   # delta from O recomputed as P V in FP32 inside the backward
 DELTA_FROM_DP_P = 2           # delta = rowsum(dP o P), no output read
 _lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
+_lib.fa_delta_error_split.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
 _lib.fa_profile_stop.argtypes = [_i, _P, _P]
@@ -57,7 +58,7 @@ _lib.fa_last_error.restype = ctypes.c_char_p
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
-            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex):
+            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex, _lib.fa_delta_error_split):
     _fn.restype = ctypes.c_int
 
 
@@ -176,6 +177,14 @@ def fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tie_count, pv_e
     return _check("fa_tie_stats_ex", rc) if check else rc
 
 
+def fa_delta_error_split(q, k, v, o, dO, B, H, N, d, causal, scale, mode, err_one, err_rest, err_out,
+                         beta=None, eps=None, stream=None, check=True):
+    rc = _lib.fa_delta_error_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), B, H, N, d, int(causal),
+                                   float(scale), int(mode), _params(beta, eps), _ptr(err_one), _ptr(err_rest),
+                                   _ptr(err_out), _stream(stream))
+    return _check("fa_delta_error_split", rc) if check else rc
+
+
 def fa_device_status(stream=None, reset=True) -> int:
     return int(_lib.fa_device_status(_stream(stream), int(reset)))
 
@@ -253,3 +262,16 @@ def delta_error(q, k, v, o, dO, causal=True, scale=None, mode=0, stream=None, be
     fa_tie_stats_ex(q, k, v, o, B, H, N, d, causal, scale, mode, tc, pe, None, dO=dO, delta_err=de, beta=beta,
                     stream=stream)
     return de
+
+
+def delta_error_split(q, k, v, o, dO, causal=True, scale=None, mode=0, stream=None, beta=None, eps=None):
+    """(err_one, err_rest, err_out), FP32 [B, H, N]: delta_lp - delta_hp of the
+    stored output o split into keys with BF16 probability 1, the other keys,
+    and the output rounding (fa_delta_error_split)."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    outs = [torch.empty((B, H, N), device=q.device, dtype=torch.float32) for _ in range(3)]
+    fa_delta_error_split(q, k, v, o, dO, B, H, N, d, causal, scale, mode, *outs, beta=beta, eps=eps,
+                         stream=stream)
+    return tuple(outs)

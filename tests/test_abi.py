@@ -19,7 +19,7 @@ def test_library_exports_every_declared_symbol():
     declared = fa.declared_symbols()
     assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
                              "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc",
-                             "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex"}
+                             "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex", "fa_delta_error_split"}
     lib = ctypes.CDLL(fa.library_path())
     for name in declared:
         assert hasattr(lib, name), name

@@ -442,3 +442,55 @@ def test_near_tie_shift_keeps_the_exact_output():
         np.testing.assert_allclose(f["lse"], base["lse"], rtol=0, atol=1e-12)
     with pytest.raises(ValueError):
         orc.fwd(q, k, v, 0, 1.0, 1, eps=-1e-3)
+
+
+# ---- decomposition of the delta error (delta_lp - delta_hp) -------------------
+
+def test_delta_split_sums_to_the_delta_error():
+    # one + rest + out = sum_c dO (o - O_hp) for any stored output o, by
+    # construction; checked with an arbitrary o and the oracle's exact O_hp
+    from precision_flash_attention_attn_gb300.inputs import make_case
+    c = make_case("tiny")
+    BH = c.B * c.H
+    qf, kf, vf, gf = (c.f64(n).reshape(BH, c.N, c.d).astype(np.float32) for n in ("q", "k", "v", "do"))
+    ex = orc.fwd(qf, kf, vf, c.causal, c.scale, 0)
+    rng = np.random.default_rng(9)
+    o = (ex["o"] + rng.standard_normal(ex["o"].shape) * 1e-2).astype(np.float32)
+    want = (gf.astype(np.float64) * (o.astype(np.float64) - ex["o"])).sum(-1)
+    for mode in (0, 1, 2):
+        sp = orc.delta_split(qf, kf, vf, o, gf, c.causal, c.scale, mode)
+        np.testing.assert_allclose(sp["one"] + sp["rest"] + sp["out"], want, rtol=0, atol=1e-12)
+
+
+def test_delta_split_uniform_row():
+    # all scores equal and zero: every Pbar is exactly 1 in the baseline, so
+    # nothing falls in `rest`; b_j / l = 1/n = p_j, so `one` is 0 too, and the
+    # whole error is the output's own rounding
+    N, d = 8, 4
+    q = np.zeros((1, N, d), np.float32)
+    k = np.zeros((1, N, d), np.float32)
+    v = np.random.default_rng(3).standard_normal((1, N, d)).astype(np.float32)
+    g = np.random.default_rng(4).standard_normal((1, N, d)).astype(np.float32)
+    o = np.random.default_rng(5).standard_normal((1, N, d)).astype(np.float32)
+    sp = orc.delta_split(q, k, v, o, g, 0, 0.5, 0)
+    assert np.all(sp["one"] == 0.0) and np.all(sp["rest"] == 0.0)
+    want = (g.astype(np.float64) * (o.astype(np.float64) - v.astype(np.float64).mean(1, keepdims=True))).sum(-1)
+    np.testing.assert_allclose(sp["out"], want, rtol=0, atol=1e-12)
+
+
+def test_delta_split_stabilised_tied_row_has_no_unit_part():
+    # a row whose maximum rm > 0 is tied: the stabilised shift 2*rm puts
+    # every Pbar below 1 (here exp(-1) at most), so `one` is exactly 0, while
+    # the baseline feeds 1.0 on both tied keys and `one` is not 0
+    N, d = 6, 4
+    q = np.zeros((1, N, d), np.float32)
+    q[0, :, 0] = 1.0
+    k = np.zeros((1, N, d), np.float32)
+    k[0, :, 0] = [2.0, 0.5, 2.0, -1.0, 1.0, 0.25]
+    v = np.random.default_rng(6).standard_normal((1, N, d)).astype(np.float32)
+    g = np.random.default_rng(7).standard_normal((1, N, d)).astype(np.float32)
+    o = np.random.default_rng(8).standard_normal((1, N, d)).astype(np.float32)
+    s1 = orc.delta_split(q, k, v, o, g, 0, 0.5, 1)
+    s0 = orc.delta_split(q, k, v, o, g, 0, 0.5, 0)
+    assert np.all(s1["one"] == 0.0)
+    assert np.all(s0["one"] != 0.0)

@@ -189,3 +189,39 @@ def test_beta_sweep_runs_on_tiny(fa, capsys):
     for ln in lines[1:]:
         assert ln["p_one1_mean"] < lines[0]["p_one1_mean"]
         assert ln["nonfinite_rows"] == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_delta_error_split_matches_oracle(fa, mode):
+    # the decomposition of delta_lp - delta_hp (keys with BF16 probability 1,
+    # the rest, the output rounding) for an output produced by the oracle's
+    # emulation, against the oracle's FP64 decomposition of the same output;
+    # the three parts add up to the statistics kernel's delta_err
+    import torch
+    c = case("tiny")
+    qf, kf, vf = _arrays(c)
+    gf = f32(c.do).reshape(c.B * c.H, c.N, c.d)
+    em = orc.fwd_emul(qf, kf, vf, c.causal, c.scale, mode, block_n=128)
+    o_in = em["o"].reshape(c.q.shape)
+    if mode == 2:
+        o_dev = torch.from_numpy(o_in.astype(np.float32)).cuda()
+    else:
+        o_dev = dev_bf16(bf16_bits(o_in.astype(np.float32)))
+    q, k, v, g = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    one, rest, out = (t.cpu().numpy().reshape(-1).astype(np.float64)
+                      for t in fa.delta_error_split(q, k, v, o_dev, g, c.causal, c.scale, mode))
+    de = fa.delta_error(q, k, v, o_dev, g, c.causal, c.scale, mode).cpu().numpy().reshape(-1)
+    assert fa.fa_device_status() == 0
+    want = orc.delta_split(qf, kf, vf, o_in.reshape(qf.shape).astype(np.float32), gf, c.causal, c.scale, mode)
+    tol = 2e-4 * max(1.0, np.abs(gf).max())
+    np.testing.assert_allclose(one, want["one"].reshape(-1), rtol=0, atol=tol)
+    np.testing.assert_allclose(rest, want["rest"].reshape(-1), rtol=0, atol=tol)
+    np.testing.assert_allclose(out, want["out"].reshape(-1), rtol=0, atol=tol)
+    np.testing.assert_allclose(one + rest + out, de, rtol=0, atol=tol)
+    if mode == 1:
+        # no key of a tied row with a non-tiny positive or negative maximum
+        # keeps probability 1, so the unit part vanishes there
+        tied = np.flatnonzero(c.planted.reshape(-1) & (c.ties.reshape(-1) > 1))
+        s_max = np.array([(kf[r // c.N, : r % c.N + 1] @ qf[r // c.N, r % c.N]).max() for r in tied])
+        keep = tied[np.abs(c.scale * s_max) > 2.0 ** -8]
+        assert keep.size > 20 and np.all(one[keep] == 0.0)
