@@ -185,6 +185,34 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               int delta_source, fa_stream_t stream);
 
 /*
+ * Per-head modes (section 5, "Head-wise high-precision substitution": the
+ * FP32 output only for the heads implicated in the failure).
+ *
+ * fa_fwd_heads -- the forward with a mode per head: head_modes is a host
+ * array of H entries in {FA_MODE_BASELINE, FA_MODE_STABILISED,
+ * FA_MODE_FP32_OUT}, the same for every batch; H <= 64 (FA_ERR_UNSUPPORTED
+ * above).  The heads in modes 0 and 1 write BF16 O into o_bf16, those in mode
+ * 2 FP32 O into o_fp32; both buffers are full [B,H,N,d] tensors of which only
+ * their heads' slices are written (either may be NULL if no head uses it).
+ * lse is written for every head.  params as fa_fwd_ex (used by mode-1 heads).
+ * One forward launch per mode present, each over its own heads.
+ *
+ * fa_bwd_heads -- the matching backward: delta = rowsum(dO o O) of each head
+ * from its own stored output (o_fp32 for mode-2 heads, o_bf16 otherwise);
+ * everything else as fa_bwd (same workspace, one launch).
+ *
+ * Errors as fa_fwd / fa_bwd; FA_ERR_INVALID_ARG for a NULL head_modes or an
+ * entry out of range.
+ */
+int fa_fwd_heads(const void* q, const void* k, const void* v, void* o_bf16, float* o_fp32,
+                 float* lse, int B, int H, int N, int d, int causal, float scale,
+                 const int* head_modes, const fa_stab_params_t* params, fa_stream_t stream);
+int fa_bwd_heads(const void* q, const void* k, const void* v, const void* o_bf16,
+                 const float* o_fp32, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                 float scale, const int* head_modes, fa_stream_t stream);
+
+/*
  * fa_bwd_noalloc -- the same backward as fa_bwd, for callers that must not
  * allocate device memory: code that runs after a framework's caching
  * allocator has reserved (nearly) all of the GPU's memory, so a driver

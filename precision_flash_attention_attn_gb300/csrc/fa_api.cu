@@ -189,7 +189,8 @@ bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o,
 // zero region at zero again.  Arguments are already validated.
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
-                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0) {
+                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0,
+                    const float* o32 = nullptr, uint64_t fp32_mask = 0) {
     const int BH = B * H;
     const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
     char* zb = static_cast<char*>(zero);
@@ -223,6 +224,9 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     a.sync = sync;
     a.clean = clean;
     a.delta_given = delta_given;
+    a.o32 = o32;
+    a.fp32_mask = fp32_mask;
+    a.H = H;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -300,16 +304,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, mode, nullptr, stream);
 }
 
-int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-              int causal, float scale, int mode, const fa_stab_params_t* params, fa_stream_t stream) {
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return FA_ERR_INVALID_ARG;
-    int rc = check_common(B, H, N, d, causal, scale, mode);
-    if (rc) return rc;
-    float beta = 0.f, eps = 0.f;
-    if ((rc = check_params(params, &beta, &eps))) return rc;
-    DeviceInfo* di = nullptr;
-    if ((rc = device_info(&di))) return rc;
+}  // extern "C"
+
+namespace {
+
+// The forward of one mode over the heads in head_mask (~0: all), arguments
+// already validated.
+int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                int causal, float scale, int mode, float beta, float eps, uint64_t head_mask, const DeviceInfo* di,
+                cudaStream_t st) {
     const int BH = B * H;
     CUtensorMap mq, mk, mv, mo;
     // O as a TMA store target: 64 BF16 or 32 FP32 columns (128 bytes) per box row
@@ -337,9 +340,10 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.beta = beta;
     a.status = di->status;
     a.num_sms = di->num_sms;
+    a.head_mask = head_mask;
+    a.H = H;
     const char* hook = std::getenv("FA_TEST_WITHHOLD_K");
     a.test_withhold_k = (hook && hook[0] == '1') ? 1 : 0;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (mode != FA_MODE_STABILISED || eps == 0.f)
         return fa::launch_fwd(a, false, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     // A tolerance: each row's shift from a pre-pass over the whole row, held
@@ -352,10 +356,66 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         return FA_ERR_ALLOC;
     }
     a.shift = static_cast<float*>(ws);
-    rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, static_cast<float*>(ws), nullptr, st);
+    int rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, static_cast<float*>(ws), nullptr, st);
     if (rc == FA_OK && fa::launch_fwd(a, false, st) != cudaSuccess) rc = FA_ERR_CUDA;
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(row shifts)", fe);
+    return rc;
+}
+
+// Per-head modes: each of the H entries in {0, 1, 2}, H <= 64.  Sets the
+// masks of the heads computed in each mode.
+int check_head_modes(const int* head_modes, int H, uint64_t mask[3]) {
+    mask[0] = mask[1] = mask[2] = 0;
+    if (!head_modes) return FA_ERR_INVALID_ARG;
+    if (H > 64) {
+        fa::set_error_msg("per-head modes", "at most 64 heads per batch");
+        return FA_ERR_UNSUPPORTED;
+    }
+    for (int h = 0; h < H; ++h) {
+        if (head_modes[h] < 0 || head_modes[h] > 2) return FA_ERR_INVALID_ARG;
+        mask[head_modes[h]] |= 1ull << h;
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+              int causal, float scale, int mode, const fa_stab_params_t* params, fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    return run_forward(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta, eps, ~0ull, di,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_heads(const void* q, const void* k, const void* v, void* o_bf16, float* o_fp32, float* lse, int B,
+                 int H, int N, int d, int causal, float scale, const int* head_modes,
+                 const fa_stab_params_t* params, fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, 0);
+    if (rc) return rc;
+    uint64_t mask[3];
+    if ((rc = check_head_modes(head_modes, H, mask))) return rc;
+    if (((mask[0] | mask[1]) && !aligned16(o_bf16)) || (mask[2] && !aligned16(o_fp32))) return FA_ERR_INVALID_ARG;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int mode = 0; mode < 3 && rc == FA_OK; ++mode) {
+        if (!mask[mode]) continue;
+        void* o = (mode == 2) ? static_cast<void*>(o_fp32) : o_bf16;
+        rc = run_forward(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta, eps, mask[mode], di, st);
+    }
     return rc;
 }
 
@@ -387,6 +447,46 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
                              static_cast<char*>(ws) + z.zero_bytes(), 0, st);
+    const cudaError_t fe = cudaFreeAsync(ws, st);
+    if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
+    return rc;
+}
+
+int fa_bwd_heads(const void* q, const void* k, const void* v, const void* o_bf16, const float* o_fp32,
+                 const float* lse, const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 int causal, float scale, const int* head_modes, fa_stream_t stream) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, 0);
+    if (rc) return rc;
+    uint64_t mask[3];
+    if ((rc = check_head_modes(head_modes, H, mask))) return rc;
+    if (((mask[0] | mask[1]) && !aligned16(o_bf16)) || (mask[2] && !aligned16(o_fp32))) return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const BwdSizes z = bwd_sizes(B * H, N, d);
+    const size_t ws_bytes = z.zero_bytes() + z.row_bytes();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
+    if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    reserve_pool(di, ws_bytes);
+    void* ws = nullptr;
+    cudaError_t ae = cudaMallocAsync(&ws, ws_bytes, st);
+    if (ae != cudaSuccess || !ws) {
+        fa::set_error("cudaMallocAsync(workspace)", ae);
+        cudaGetLastError();
+        return FA_ERR_ALLOC;
+    }
+    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
+    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
+    // delta of each head from its own stored output: o_fp32 for the heads in
+    // mode 2, o_bf16 for the others (a head's o is never read otherwise)
+    const void* o_any = (mask[0] | mask[1]) ? o_bf16 : static_cast<const void*>(o_fp32);
+    if (rc == FA_OK)
+        rc = launch_backward(q, k, v, o_any, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, 0, di, ws,
+                             static_cast<char*>(ws) + z.zero_bytes(), 0, st, 0, o_fp32,
+                             mask[2] ? mask[2] : 0);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;

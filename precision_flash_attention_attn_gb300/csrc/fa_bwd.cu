@@ -53,6 +53,9 @@ struct BwdParams {
     uint32_t* sync;       // grid barrier words (zero before the first launch)
     int clean;            // 1: leave the accumulator and the barrier words at zero afterwards
     int delta_given;      // 1: delta already holds -alpha*rowsum(dP o P); phase A forms lse2 only
+    const float* o32;     // per-head modes: FP32 O of the heads in fp32_mask (o holds the others)
+    uint64_t fp32_mask;
+    int H;
     int BH, N, Npad, mode;
     int n_kt;     // key tiles per (batch, head)
     int n_items;  // BH * n_kt
@@ -68,9 +71,12 @@ constexpr uint32_t kBarGo = 2;       // named barrier: phase C may start (math +
 // D/8 threads per row, 8 elements (16 bytes of dO) each; each thread takes
 // kUnroll rows, a grid stride apart, per step, and every load of a step (dO,
 // O and the LSE) is issued before any is used, so a step costs one memory
-// round trip.  O32: O is FP32 (mode 2).
+// round trip.  O32: O is FP32 (mode 2).  sel < 0: every row; sel = 0 / 1:
+// only the rows of heads outside / inside fp32_mask (per-head modes), whose
+// O is read from o (BF16) / o32 (FP32).
 template <int D, bool O32>
-__device__ __forceinline__ void prepare_rows(const BwdParams& p) {
+__device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
+    const void* obase = (sel == 1) ? static_cast<const void*>(p.o32) : p.o;
     constexpr int TPR = D / 8;                  // threads per row
     constexpr int RPC = kBwdThreads / TPR;      // rows per CTA and step
     constexpr int kUnroll = O32 ? 5 : 7;
@@ -83,13 +89,14 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p) {
     for (int r0 = static_cast<int>(blockIdx.x) * RPC + tid / TPR; r0 < rows; r0 += kUnroll * stride) {
         uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
         float lse[kUnroll];
-        bool valid[kUnroll];
+        bool valid[kUnroll], chosen[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int r = r0 + u * stride;
             const int bh = r / p.Npad;
             const int i = r - bh * p.Npad;
-            valid[u] = r < rows && i < p.N;
+            chosen[u] = r < rows && (sel < 0 || static_cast<int>((p.fp32_mask >> (bh % p.H)) & 1ull) == sel);
+            valid[u] = chosen[u] && i < p.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
             lse[u] = 0.f;
             if (valid[u] && p.delta_given) {
@@ -99,10 +106,10 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p) {
                 const size_t base = row * D + sub * 8;
                 g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
                 if (O32) {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.o) + base);
-                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.o) + base + 4);
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
+                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base + 4);
                 } else {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + base);
+                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(obase) + base);
                 }
                 if (sub == 0) lse[u] = p.lse[row];
             }
@@ -129,7 +136,7 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p) {
 #pragma unroll
             for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             const int r = r0 + u * stride;
-            if (sub == 0 && r < rows) {
+            if (sub == 0 && chosen[u]) {
                 // stored pre-negated / pre-scaled for the main phase's FMAs:
                 //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
                 //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
@@ -316,10 +323,14 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     // Phase A.  Nothing above reads or writes global memory, so under
     // programmatic dependent launch all of it overlaps the previous kernel.
     griddep_wait();
-    if (p.mode == 2)
-        prepare_rows<D, true>(p);
-    else
-        prepare_rows<D, false>(p);
+    if (p.fp32_mask != 0) {  // per-head modes: each head's delta from its own stored O
+        prepare_rows<D, false>(p, 0);
+        prepare_rows<D, true>(p, 1);
+    } else if (p.mode == 2) {
+        prepare_rows<D, true>(p, -1);
+    } else {
+        prepare_rows<D, false>(p, -1);
+    }
     const bool started = grid_barrier(p.sync, p.status);
 
     if (started) {
@@ -837,6 +848,9 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.sync = a.sync;
     p.clean = a.clean;
     p.delta_given = a.delta_given;
+    p.o32 = a.o32;
+    p.fp32_mask = a.fp32_mask;
+    p.H = a.H > 0 ? a.H : 1;
     p.mode = a.mode;
     p.BH = a.BH;
     p.N = a.N;

@@ -118,6 +118,8 @@ struct FwdParams {
     int test_withhold_k;  // test hook (see FwdArgs)
     const float* shift;   // mode 1, nullable: fixed per-row shift (see FwdArgs)
     const int32_t* rs_in; // statistics variant, nullable: tie counts to report
+    uint64_t head_mask;   // heads h (bit h) this launch computes; ~0: all
+    int H;
 };
 
 // Work items are (query-tile group, batch-head) pairs, numbered longest first
@@ -155,15 +157,20 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
     auto item_bh = [&](int it) { return it % p.BH; };
     auto item_cq = [&](int it) { return p.n_cq - 1 - it / p.BH; };
     auto tile_q0 = [&](int cq, int t) { return (cq * NQ + t) * kBlockM; };
-    auto tile_nkt = [&](int cq, int t) {
-        const int qt = cq * NQ + t;
-        if (qt * kBlockM >= p.N) return 0;
+    // heads outside this launch's set are handled like tiles past N: nothing
+    // is loaded, computed or stored for them
+    auto head_on = [&](int it) {
+        return p.head_mask == ~0ull || ((p.head_mask >> ((it % p.BH) % p.H)) & 1ull) != 0;
+    };
+    auto tile_nkt = [&](int it, int t) {
+        const int qt = item_cq(it) * NQ + t;
+        if (qt * kBlockM >= p.N || !head_on(it)) return 0;
         return CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all;
     };
-    auto item_nkt = [&](int cq) {
+    auto item_nkt = [&](int it) {
         int n = 0;
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) n = tile_nkt(cq, t) > n ? tile_nkt(cq, t) : n;
+        for (int t = 0; t < NQ; ++t) n = tile_nkt(it, t) > n ? tile_nkt(it, t) : n;
         return n;
     };
 
@@ -224,15 +231,15 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     if (n >= QB) ok = mbar_wait(bar(L::kQEmpty + qb), (uq - 1) & 1u, p.status);
                     if (!ok) break;
                     int n_active = 0;
-                    for (int t = 0; t < NQ; ++t) n_active += tile_nkt(cq, t) > 0 ? 1 : 0;
+                    for (int t = 0; t < NQ; ++t) n_active += tile_nkt(it, t) > 0 ? 1 : 0;
                     mbar_arrive_expect_tx(bar(L::kQFull + qb), L::kTileBytes * n_active);
                     for (int t = 0; t < NQ; ++t) {
-                        if (tile_nkt(cq, t) == 0) continue;
+                        if (tile_nkt(it, t) == 0) continue;
                         for (int b = 0; b < D / 64; ++b)
                             tma_load_3d(sb + L::kQ + (qb * NQ + t) * L::kTileBytes + b * 16384, &tm_q,
                                         bar(L::kQFull + qb), b * 64, tile_q0(cq, t), bh);
                     }
-                    const int n_kt = item_nkt(cq);
+                    const int n_kt = item_nkt(it);
                     for (int j = 0; j < n_kt; ++j, ++g) {
                         const int s = g % S;
                         const uint32_t u = static_cast<uint32_t>(g / S);
@@ -325,9 +332,8 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
             for (int r = 0, n = 0; ok; ++r, ++n) {
                 const int it = fwd_item(r);
                 if (it >= p.n_items) break;
-                const int cq = item_cq(it);
-                const int nkt = tile_nkt(cq, t);
-                const int n_kt = item_nkt(cq);
+                const int nkt = tile_nkt(it, t);
+                const int n_kt = item_nkt(it);
                 const int qb = n % QB;
                 const uint32_t q_sm = sb + L::kQ + (qb * NQ + t) * L::kTileBytes;
                 if (nkt > 0) ok = wait_all(bar(L::kQFull + qb), static_cast<uint32_t>(n / QB) & 1u);
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
             const int it = fwd_item(r);
             if (it >= p.n_items) break;
             const int bh = item_bh(it), cq = item_cq(it);
-            const int nkt = tile_nkt(cq, t);
+            const int nkt = tile_nkt(it, t);
             if (nkt == 0) continue;
             const int q0 = tile_q0(cq, t);
             const int qrow = q0 + row;
@@ -754,6 +760,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.test_withhold_k = a.test_withhold_k;
     p.shift = a.shift;
     p.rs_in = a.rs_in;
+    p.head_mask = a.head_mask;
+    p.H = a.H > 0 ? a.H : 1;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
     p.n_cq = (n_qt + NQ - 1) / NQ;
     p.n_items = a.BH * p.n_cq;

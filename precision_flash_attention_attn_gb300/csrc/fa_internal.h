@@ -31,6 +31,8 @@ struct FwdArgs {
     const float* shift;   // nullable, mode 1: fixed per-row shift [BH, N] (raw
                           // score units) used from the first key tile on
     const int32_t* rs_in; // nullable, statistics variant: tie counts to report
+    uint64_t head_mask = ~0ull;  // heads h (bit h, h < 64) computed by this launch; ~0: all
+    int H = 0;                   // heads per batch (for head_mask)
 };
 
 // Row statistics pre-pass of the stabilised softmax with a tolerance eps:
@@ -77,6 +79,9 @@ struct BwdArgs {
     uint32_t* sync;               // grid barrier words, zero before the first launch
     int clean;                    // 1: leave dq_acc at zero when done
     int delta_given;              // 1: delta is already in place (rowsum(dP o P) pre-pass)
+    const float* o32 = nullptr;   // per-head modes: FP32 O of the heads in fp32_mask
+    uint64_t fp32_mask = 0;       // heads h (bit h) whose delta uses o32 instead of o
+    int H = 0;
     void* dq;                     // [BH, N, d] BF16
     void* dk;
     void* dv;

@@ -50,6 +50,8 @@ DELTA_RECOMPUTED_O_FP32 = 1   # delta from O recomputed as P V in FP32 inside th
 DELTA_FROM_DP_P = 2           # delta = rowsum(dP o P), no output read
 _lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
 _lib.fa_delta_error_split.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P]
+_lib.fa_fwd_heads.argtypes = [_P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _P, _SP, _P]
+_lib.fa_bwd_heads.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
 _lib.fa_profile_start.argtypes = []
 _lib.fa_profile_stop.argtypes = [_i, _P, _P]
@@ -58,7 +60,8 @@ _lib.fa_last_error.restype = ctypes.c_char_p
 _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
-            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex, _lib.fa_delta_error_split):
+            _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex, _lib.fa_delta_error_split,
+            _lib.fa_fwd_heads, _lib.fa_bwd_heads):
     _fn.restype = ctypes.c_int
 
 
@@ -183,6 +186,30 @@ def fa_delta_error_split(q, k, v, o, dO, B, H, N, d, causal, scale, mode, err_on
                                    float(scale), int(mode), _params(beta, eps), _ptr(err_one), _ptr(err_rest),
                                    _ptr(err_out), _stream(stream))
     return _check("fa_delta_error_split", rc) if check else rc
+
+
+def _head_modes(head_modes):
+    arr = (ctypes.c_int * len(head_modes))(*[int(m) for m in head_modes])
+    return arr
+
+
+def fa_fwd_heads(q, k, v, o_bf16, o_fp32, lse, B, H, N, d, causal, scale, head_modes, beta=None, eps=None,
+                 stream=None, check=True):
+    """Forward with a mode per head (host list of H modes)."""
+    hm = _head_modes(head_modes)
+    rc = _lib.fa_fwd_heads(_ptr(q), _ptr(k), _ptr(v), _ptr(o_bf16), _ptr(o_fp32), _ptr(lse), B, H, N, d,
+                           int(causal), float(scale), ctypes.cast(hm, _P), _params(beta, eps), _stream(stream))
+    return _check("fa_fwd_heads", rc) if check else rc
+
+
+def fa_bwd_heads(q, k, v, o_bf16, o_fp32, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, head_modes,
+                 stream=None, check=True):
+    """Backward with a mode per head: delta from each head's own output."""
+    hm = _head_modes(head_modes)
+    rc = _lib.fa_bwd_heads(_ptr(q), _ptr(k), _ptr(v), _ptr(o_bf16), _ptr(o_fp32), _ptr(lse), _ptr(dO), _ptr(dq),
+                           _ptr(dk), _ptr(dv), B, H, N, d, int(causal), float(scale), ctypes.cast(hm, _P),
+                           _stream(stream))
+    return _check("fa_bwd_heads", rc) if check else rc
 
 
 def fa_device_status(stream=None, reset=True) -> int:

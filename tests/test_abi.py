@@ -19,7 +19,8 @@ def test_library_exports_every_declared_symbol():
     declared = fa.declared_symbols()
     assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
                              "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc",
-                             "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex", "fa_delta_error_split"}
+                             "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex", "fa_delta_error_split",
+                             "fa_fwd_heads", "fa_bwd_heads"}
     lib = ctypes.CDLL(fa.library_path())
     for name in declared:
         assert hasattr(lib, name), name
@@ -171,3 +172,37 @@ def test_bwd_ex_invalid_arguments(source, kw):
 
 def test_bwd_ex_stored_o_still_needs_o():
     assert _bwd_ex(0, o=0) == 1
+
+
+def _fwd_heads(modes, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o_bf16=FAKE, o_fp32=FAKE, lse=FAKE, B=1, H=len(modes), N=128, d=64, causal=1,
+             scale=0.125, head_modes=modes, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_fwd_heads(**a)
+
+
+def _bwd_heads(modes, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o_bf16=FAKE, o_fp32=FAKE, lse=FAKE, dO=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1,
+             H=len(modes), N=128, d=64, causal=1, scale=0.125, head_modes=modes, stream=0, check=False)
+    a.update(kw)
+    return fa.fa_bwd_heads(**a)
+
+
+@pytest.mark.parametrize("modes", [[0, 3], [-1, 1], [2, 2, 7]])
+def test_head_modes_out_of_range(modes):
+    assert _fwd_heads(modes) == 1
+    assert _bwd_heads(modes) == 1
+
+
+def test_head_modes_need_their_output_buffer():
+    # BF16 heads need o_bf16, FP32 heads o_fp32; an unused one may be NULL
+    assert _fwd_heads([0, 2], o_bf16=0) == 1
+    assert _fwd_heads([0, 2], o_fp32=0) == 1
+    assert _bwd_heads([1, 2], o_fp32=MISALIGNED) == 1
+    assert _fwd_heads([2, 2], o_bf16=0) not in (1, 2)
+    assert _fwd_heads([0, 1], o_fp32=0) not in (1, 2)
+
+
+def test_head_modes_at_most_64_heads():
+    assert _fwd_heads([0] * 65) == 2
+    assert _bwd_heads([2] * 65) == 2
