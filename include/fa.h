@@ -185,6 +185,25 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               int delta_source, fa_stream_t stream);
 
 /*
+ * Layouts of the [*, N, d] tensors (q, k, v, o, dO, dq, dk, dv; lse stays
+ * [B, H, N]):
+ *   FA_LAYOUT_BHND  [B, H, N, d] contiguous (what every other entry point takes)
+ *   FA_LAYOUT_BNHD  [B, N, H, d] contiguous (heads interleaved per position, as
+ *                   a projection's output is laid out before any transpose)
+ * fa_fwd_layout / fa_bwd_layout -- fa_fwd_ex / fa_bwd with a layout; the
+ * kernels address the tensors in place (4-D tensor maps; no copy).
+ * FA_ERR_INVALID_ARG for an unknown layout.  Otherwise as fa_fwd_ex / fa_bwd.
+ */
+enum { FA_LAYOUT_BHND = 0, FA_LAYOUT_BNHD = 1 };
+int fa_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int N, int d, int causal, float scale, int mode,
+                  const fa_stab_params_t* params, int layout, fa_stream_t stream);
+int fa_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv,
+                  int B, int H, int N, int d, int causal, float scale, int mode,
+                  int layout, fa_stream_t stream);
+
+/*
  * Per-head modes (section 5, "Head-wise high-precision substitution": the
  * FP32 output only for the heads implicated in the failure).
  *

@@ -121,6 +121,65 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     return FA_OK;
 }
 
+// Row strides of the [*, N, d] tensors in a layout (FA_LAYOUT_*).
+fa::RowLayout layout_of(int layout, int H, int N, int d) {
+    fa::RowLayout l{};
+    l.H = H;
+    if (layout == FA_LAYOUT_BNHD) {
+        l.head_inner = 1;
+        l.sN = static_cast<long long>(H) * d;
+        l.sH = d;
+        l.sB = static_cast<long long>(N) * H * d;
+    } else {
+        l.head_inner = 0;
+        l.sN = d;
+        l.sH = static_cast<long long>(N) * d;
+        l.sB = static_cast<long long>(H) * N * d;
+    }
+    return l;
+}
+
+// 4-D view of a [*, N, d] tensor in layout `lay`, dimensions in increasing
+// stride order (see fa::RowLayout); box = inner x rows (x 1 head x 1 batch),
+// 128-byte swizzle (inner * elem_bytes == 128).
+int make_rows_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, const fa::RowLayout& lay,
+                  int B, int N, int d, int inner, int rows = fa::kBlockM) {
+    const cuuint64_t e = static_cast<cuuint64_t>(elem_bytes);
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    dims[0] = static_cast<cuuint64_t>(d);
+    dims[3] = static_cast<cuuint64_t>(B);
+    strides[2] = static_cast<cuuint64_t>(lay.sB) * e;
+    box[0] = static_cast<cuuint32_t>(inner);
+    box[3] = 1;
+    if (lay.head_inner) {
+        dims[1] = static_cast<cuuint64_t>(lay.H);
+        dims[2] = static_cast<cuuint64_t>(N);
+        strides[0] = static_cast<cuuint64_t>(lay.sH) * e;
+        strides[1] = static_cast<cuuint64_t>(lay.sN) * e;
+        box[1] = 1;
+        box[2] = static_cast<cuuint32_t>(rows);
+    } else {
+        dims[1] = static_cast<cuuint64_t>(N);
+        dims[2] = static_cast<cuuint64_t>(lay.H);
+        strides[0] = static_cast<cuuint64_t>(lay.sN) * e;
+        strides[1] = static_cast<cuuint64_t>(lay.sH) * e;
+        box[1] = static_cast<cuuint32_t>(rows);
+        box[2] = 1;
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[64];
+        snprintf(msg, sizeof msg, "CUresult %d", static_cast<int>(r));
+        fa::set_error_msg("cuTensorMapEncodeTiled", msg);
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
 // Stabilised-softmax parameters (NULL: the defaults).  "The modified safe
 // softmax" of section 3.4.5 requires beta > 1 and a tolerance eps >= 0.
 int check_params(const fa_stab_params_t* prm, float* beta, float* eps) {
@@ -136,8 +195,9 @@ int check_params(const fa_stab_params_t* prm, float* beta, float* eps) {
 
 // Enqueue the row pre-pass (row maximum, near-tie count, shift).
 int launch_row_pass(const void* q, const void* k, int BH, int N, int d, int causal, float scale, int mode,
-                    float beta, float eps, float* shift, int32_t* rs, cudaStream_t st) {
+                    float beta, float eps, float* shift, int32_t* rs, cudaStream_t st, const fa::RowLayout& lay) {
     fa::RowShiftArgs r{};
+    r.lay = lay;
     r.q = q;
     r.k = k;
     r.shift = shift;
@@ -190,8 +250,9 @@ bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o,
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
                     const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0,
-                    const float* o32 = nullptr, uint64_t fp32_mask = 0) {
+                    const float* o32 = nullptr, uint64_t fp32_mask = 0, int layout = FA_LAYOUT_BHND) {
     const int BH = B * H;
+    const fa::RowLayout lay = layout_of(layout, H, N, d);
     const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
     char* zb = static_cast<char*>(zero);
     uint32_t* sync = reinterpret_cast<uint32_t*>(zb);
@@ -199,13 +260,13 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     float* lse2 = static_cast<float*>(rows);
     float* delta = lse2 + static_cast<size_t>(BH) * Npad;
     CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
-    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
+    if (make_rows_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mdo, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
         make_map(&macc, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 32) ||
-        make_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32) ||
-        make_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 32))
+        make_rows_map(&mdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64, 32) ||
+        make_rows_map(&mdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64, 32))
         return FA_ERR_CUDA;
     fa::BwdArgs a{};
     a.tm_q = &mq;
@@ -227,6 +288,7 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     a.o32 = o32;
     a.fp32_mask = fp32_mask;
     a.H = H;
+    a.lay = lay;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;
@@ -312,16 +374,17 @@ namespace {
 // already validated.
 int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                 int causal, float scale, int mode, float beta, float eps, uint64_t head_mask, const DeviceInfo* di,
-                cudaStream_t st) {
+                cudaStream_t st, int layout = FA_LAYOUT_BHND) {
     const int BH = B * H;
+    const fa::RowLayout lay = layout_of(layout, H, N, d);
     CUtensorMap mq, mk, mv, mo;
     // O as a TMA store target: 64 BF16 or 32 FP32 columns (128 bytes) per box row
     const bool o32 = (mode == 2);
-    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mo, o, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o32 ? 4 : 2, BH, N,
-                 d, o32 ? 32 : 64))
+    if (make_rows_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mo, o, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o32 ? 4 : 2,
+                      lay, B, N, d, o32 ? 32 : 64))
         return FA_ERR_CUDA;
     fa::FwdArgs a{};
     a.tm_q = &mq;
@@ -342,6 +405,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
     a.num_sms = di->num_sms;
     a.head_mask = head_mask;
     a.H = H;
+    a.lay = lay;
     const char* hook = std::getenv("FA_TEST_WITHHOLD_K");
     a.test_withhold_k = (hook && hook[0] == '1') ? 1 : 0;
     if (mode != FA_MODE_STABILISED || eps == 0.f)
@@ -356,7 +420,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
         return FA_ERR_ALLOC;
     }
     a.shift = static_cast<float*>(ws);
-    int rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, static_cast<float*>(ws), nullptr, st);
+    int rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, static_cast<float*>(ws), nullptr, st, lay);
     if (rc == FA_OK && fa::launch_fwd(a, false, st) != cudaSuccess) rc = FA_ERR_CUDA;
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(row shifts)", fe);
@@ -395,6 +459,21 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     if ((rc = device_info(&di))) return rc;
     return run_forward(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta, eps, ~0ull, di,
                        static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                  int causal, float scale, int mode, const fa_stab_params_t* params, int layout, fa_stream_t stream) {
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    float beta = 0.f, eps = 0.f;
+    if ((rc = check_params(params, &beta, &eps))) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    return run_forward(q, k, v, o, lse, B, H, N, d, causal, scale, mode, beta, eps, ~0ull, di,
+                       static_cast<cudaStream_t>(stream), layout);
 }
 
 int fa_fwd_heads(const void* q, const void* k, const void* v, void* o_bf16, float* o_fp32, float* lse, int B,
@@ -447,6 +526,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
                              static_cast<char*>(ws) + z.zero_bytes(), 0, st);
+    const cudaError_t fe = cudaFreeAsync(ws, st);
+    if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
+    return rc;
+}
+
+int fa_bwd_layout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
+                  int layout, fa_stream_t stream) {
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_INVALID_ARG;
+    if (!bwd_pointers_ok(q, k, v, o, lse, dO, dq, dk, dv)) return FA_ERR_INVALID_ARG;
+    int rc = check_common(B, H, N, d, causal, scale, mode);
+    if (rc) return rc;
+    DeviceInfo* di = nullptr;
+    if ((rc = device_info(&di))) return rc;
+    const BwdSizes z = bwd_sizes(B * H, N, d);
+    const size_t ws_bytes = z.zero_bytes() + z.row_bytes();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char* fail = std::getenv("FA_TEST_FAIL_ALLOC");
+    if (fail && fail[0] == '1') return FA_ERR_ALLOC;
+    reserve_pool(di, ws_bytes);
+    void* ws = nullptr;
+    cudaError_t ae = cudaMallocAsync(&ws, ws_bytes, st);
+    if (ae != cudaSuccess || !ws) {
+        fa::set_error("cudaMallocAsync(workspace)", ae);
+        cudaGetLastError();
+        return FA_ERR_ALLOC;
+    }
+    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
+    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
+    if (rc == FA_OK)
+        rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
+                             static_cast<char*>(ws) + z.zero_bytes(), 0, st, 0, nullptr, 0, layout);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;
@@ -670,10 +781,11 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
     if ((rc = device_info(&di))) return rc;
     const int BH = B * H;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const fa::RowLayout lay = layout_of(FA_LAYOUT_BHND, H, N, d);
     CUtensorMap mq, mk, mv;
-    if (make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64) ||
-        make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64))
+    if (make_rows_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64) ||
+        make_rows_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lay, B, N, d, 64))
         return FA_ERR_CUDA;
     fa::FwdArgs a{};
     a.tm_q = &mq;
@@ -694,6 +806,8 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
     a.scale_log2 = log2e_times(scale);
     a.status = di->status;
     a.num_sms = di->num_sms;
+    a.H = H;
+    a.lay = lay;
     // A tolerance: the near-tie counts (and, in mode 1, each row's fixed
     // shift) from the row pre-pass (stream-ordered workspace, B*H*N*8 bytes).
     void* ws = nullptr;
@@ -709,7 +823,7 @@ int fa_tie_stats_ex(const void* q, const void* k, const void* v, const void* o, 
         int32_t* rs = reinterpret_cast<int32_t*>(shift + nrow);
         if (mode == FA_MODE_STABILISED) a.shift = shift;
         a.rs_in = rs;
-        rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, shift, rs, st);
+        rc = launch_row_pass(q, k, BH, N, d, causal, scale, mode, beta, eps, shift, rs, st, lay);
     }
     if (rc == FA_OK && fa::launch_fwd(a, true, st) != cudaSuccess) rc = FA_ERR_CUDA;
     if (ws) {

@@ -56,6 +56,7 @@ struct BwdParams {
     const float* o32;     // per-head modes: FP32 O of the heads in fp32_mask (o holds the others)
     uint64_t fp32_mask;
     int H;
+    RowLayout lay;        // q, k, v, o, dO, dq, dk, dv rows (the tensor maps are 4-D)
     int BH, N, Npad, mode;
     int n_kt;     // key tiles per (batch, head)
     int n_items;  // BH * n_kt
@@ -103,7 +104,7 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
                 if (sub == 0) lse[u] = p.lse[static_cast<size_t>(bh) * p.N + i];
             } else if (valid[u]) {
                 const size_t row = static_cast<size_t>(bh) * p.N + i;
-                const size_t base = row * D + sub * 8;
+                const size_t base = p.lay.row(bh, i) + sub * 8;
                 g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
                 if (O32) {
                     o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
@@ -153,34 +154,45 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
 // eight elements per thread and step, four steps' loads in flight; with
 // `clean` the accumulator is zeroed as it is read.  The loads bypass L1: the
 // accumulator was written by other SMs' reduce-adds during this launch.
-__device__ __forceinline__ void convert_dq(const BwdParams& p, size_t n8, int nthreads_cta) {
+template <int D>
+__device__ __forceinline__ void convert_dq(const BwdParams& p, int nthreads_cta) {
+    constexpr int kChunks = D / 8;  // eight-element chunks per row
     float4* acc = reinterpret_cast<float4*>(p.dq_acc);
     uint4* dq = reinterpret_cast<uint4*>(p.dq);
-    const size_t nthr = static_cast<size_t>(gridDim.x) * nthreads_cta;
-    const size_t tid = static_cast<size_t>(blockIdx.x) * nthreads_cta + threadIdx.x;
-    for (size_t e0 = tid; e0 < n8; e0 += 4 * nthr) {
+    // BH * Npad * d < 2^31 (checked on the host): 32-bit chunk indices
+    const int n8 = p.BH * p.N * kChunks;
+    const int nthr = static_cast<int>(gridDim.x) * nthreads_cta;
+    const int tid = static_cast<int>(blockIdx.x) * nthreads_cta + static_cast<int>(threadIdx.x);
+    for (int e0 = tid; e0 < n8; e0 += 4 * nthr) {
         float4 x[4], y[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const size_t e = e0 + u * nthr;
+            const int e = e0 + u * nthr;
             if (e < n8) {
-                x[u] = __ldcg(acc + 2 * e);
-                y[u] = __ldcg(acc + 2 * e + 1);
+                x[u] = __ldcg(acc + 2 * static_cast<size_t>(e));
+                y[u] = __ldcg(acc + 2 * static_cast<size_t>(e) + 1);
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const size_t e = e0 + u * nthr;
+            const int e = e0 + u * nthr;
             if (e < n8) {
                 uint4 w;
                 w.x = pack_bf16x2(x[u].x, x[u].y);
                 w.y = pack_bf16x2(x[u].z, x[u].w);
                 w.z = pack_bf16x2(y[u].x, y[u].y);
                 w.w = pack_bf16x2(y[u].z, y[u].w);
-                dq[e] = w;
+                // chunk e of the [BH, N, d] accumulator -> dq in the caller's layout
+                size_t dst = static_cast<size_t>(e);
+                if (p.lay.head_inner) {
+                    const int row = e / kChunks;
+                    const int bh = row / p.N;
+                    dst = (p.lay.row(bh, row - bh * p.N) >> 3) + static_cast<size_t>(e - row * kChunks);
+                }
+                dq[dst] = w;
                 if (p.clean) {
-                    acc[2 * e] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    acc[2 * e + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    acc[2 * static_cast<size_t>(e)] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    acc[2 * static_cast<size_t>(e) + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
         }
@@ -353,15 +365,16 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 const int itm = bwd_item(r);
                 if (itm >= p.n_items) break;
                 const int bh = item_bh(itm), kt = item_kt(itm);
+                const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
                 const int kb = n % KVB;
                 if (n >= KVB) ok = mbar_wait(bar(L::kKVEmpty + kb), static_cast<uint32_t>(n / KVB - 1) & 1u, p.status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(L::kKVFull + kb), 2 * L::kTile);
                 for (int b = 0; b < D / 64; ++b) {
-                    tma_load_3d(sb + L::kK + kb * L::kTile + b * 16384, &tm_k, bar(L::kKVFull + kb), b * 64,
-                                kt * kBlockN, bh);
-                    tma_load_3d(sb + L::kV + kb * L::kTile + b * 16384, &tm_v, bar(L::kKVFull + kb), b * 64,
-                                kt * kBlockN, bh);
+                    tma_load_rows(sb + L::kK + kb * L::kTile + b * 16384, &tm_k, bar(L::kKVFull + kb), b * 64,
+                                kt * kBlockN, hh, bb, p.lay.head_inner);
+                    tma_load_rows(sb + L::kV + kb * L::kTile + b * 16384, &tm_v, bar(L::kKVFull + kb), b * 64,
+                                kt * kBlockN, hh, bb, p.lay.head_inner);
                 }
                 const int n_iter = item_iters(kt);
                 for (int it = 0; it < n_iter; ++it, ++g) {
@@ -371,9 +384,10 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     const int q0 = (item_qt0(kt) + it) * kBlockM;
                     mbar_arrive_expect_tx(bar(L::kQFull + s), 2 * L::kTile + 1024);
                     for (int b = 0; b < D / 64; ++b) {
-                        tma_load_3d(sb + L::kQ + s * L::kTile + b * 16384, &tm_q, bar(L::kQFull + s), b * 64, q0, bh);
-                        tma_load_3d(sb + L::kDO + s * L::kTile + b * 16384, &tm_do, bar(L::kQFull + s), b * 64, q0,
-                                    bh);
+                        tma_load_rows(sb + L::kQ + s * L::kTile + b * 16384, &tm_q, bar(L::kQFull + s), b * 64, q0,
+                                      hh, bb, p.lay.head_inner);
+                        tma_load_rows(sb + L::kDO + s * L::kTile + b * 16384, &tm_do, bar(L::kQFull + s), b * 64, q0,
+                                      hh, bb, p.lay.head_inner);
                     }
                     const size_t roff = static_cast<size_t>(bh) * p.Npad + q0;
                     bulk_load(sb + L::kLse + s * 512, p.lse2 + roff, 512, bar(L::kQFull + s));
@@ -570,6 +584,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             const int itm = bwd_item(r);
             if (itm >= p.n_items) break;
             const int bh = item_bh(itm), kt = item_kt(itm);
+            const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
             const int n_iter = item_iters(kt);
             for (int it = 0; it < n_iter; ++it, ++g) {
                 ok = wait_w(bar(L::kDQFull), static_cast<uint32_t>(g) & 1u);
@@ -637,7 +652,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(which == 0 ? &tm_dv : &tm_dk, stg, b64 * 64, kt * kBlockN + wq * 32, bh);
+                        tma_store_rows(which == 0 ? &tm_dv : &tm_dk, stg, b64 * 64, kt * kBlockN + wq * 32, hh, bb, p.lay.head_inner);
                         bulk_commit();
                     }
                 }
@@ -656,7 +671,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);
         fence_async_global();
         if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
-            convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads + L::kDrainThreads);
+            convert_dq<D>(p, L::kMathThreads + L::kDrainThreads);
     }
     } else {
     regs_inc<L::kRegsMath>();
@@ -815,7 +830,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     fence_async_global();
     griddep_launch_dependents();
     if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
-        convert_dq(p, static_cast<size_t>(p.BH) * p.N * D / 8, L::kMathThreads + L::kDrainThreads);
+        convert_dq<D>(p, L::kMathThreads + L::kDrainThreads);
     }
     }  // started
 
@@ -850,7 +865,8 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.delta_given = a.delta_given;
     p.o32 = a.o32;
     p.fp32_mask = a.fp32_mask;
-    p.H = a.H > 0 ? a.H : 1;
+    p.H = a.lay.H;
+    p.lay = a.lay;
     p.mode = a.mode;
     p.BH = a.BH;
     p.N = a.N;

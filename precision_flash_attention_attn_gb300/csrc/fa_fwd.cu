@@ -111,15 +111,17 @@ struct FwdParams {
     int32_t* p_one;
     int BH, N;
     int n_cq;     // query-tile groups (of NQ tiles) per (batch, head)
-    int n_items;  // BH * n_cq work items
+    int n_items;  // BHon * n_cq work items
     float scale_log2;
     float beta;   // mode 1: shift factor of rows with a positive repeated maximum
     int* status;
     int test_withhold_k;  // test hook (see FwdArgs)
     const float* shift;   // mode 1, nullable: fixed per-row shift (see FwdArgs)
     const int32_t* rs_in; // statistics variant, nullable: tie counts to report
-    uint64_t head_mask;   // heads h (bit h) this launch computes; ~0: all
+    uint64_t head_mask;   // heads h (bit h) this launch computes
     int H;
+    int Hon, BHon;        // heads in head_mask (of H), batch x those heads
+    RowLayout lay;        // q, k, v, o rows (the tensor maps are 4-D: column, row, head, batch)
 };
 
 // Work items are (query-tile group, batch-head) pairs, numbered longest first
@@ -127,6 +129,20 @@ struct FwdParams {
 // rounds of gridDim.x: round r visits c on even rounds and gridDim.x-1-c on
 // odd ones, which balances the causal work nearly as well as greedy longest-
 // processing-time scheduling.
+// Position of the k-th (from 0) set bit of m; m has more than k set bits.
+__device__ __forceinline__ int nth_set_bit(uint64_t m, int k) {
+    uint32_t w = static_cast<uint32_t>(m);
+    int base = 0;
+    const int lo = __popc(w);
+    if (k >= lo) {
+        k -= lo;
+        w = static_cast<uint32_t>(m >> 32);
+        base = 32;
+    }
+    for (int i = 0; i < k; ++i) w &= w - 1u;  // drop the k lowest set bits
+    return base + __ffs(static_cast<int>(w)) - 1;
+}
+
 __device__ __forceinline__ int fwd_item(int r) {
     const int G = static_cast<int>(gridDim.x);
     const int c = static_cast<int>(blockIdx.x);
@@ -154,17 +170,18 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
     const int n_ktiles_all = (p.N + kBlockN - 1) / kBlockN;
     // Work item -> (batch-head, group); per query tile t of the group: first
     // row and number of key tiles it visits (0: the tile lies past N).
-    auto item_bh = [&](int it) { return it % p.BH; };
-    auto item_cq = [&](int it) { return p.n_cq - 1 - it / p.BH; };
-    auto tile_q0 = [&](int cq, int t) { return (cq * NQ + t) * kBlockM; };
-    // heads outside this launch's set are handled like tiles past N: nothing
-    // is loaded, computed or stored for them
-    auto head_on = [&](int it) {
-        return p.head_mask == ~0ull || ((p.head_mask >> ((it % p.BH) % p.H)) & 1ull) != 0;
+    // Only the heads of this launch's set are items: item x of a group is
+    // head number x % Hon of the set (in increasing h) of batch x / Hon.
+    auto item_bh = [&](int it) {
+        const int x = it % p.BHon;
+        if (p.Hon == p.H) return x;
+        return (x / p.Hon) * p.H + nth_set_bit(p.head_mask, x % p.Hon);
     };
+    auto item_cq = [&](int it) { return p.n_cq - 1 - it / p.BHon; };
+    auto tile_q0 = [&](int cq, int t) { return (cq * NQ + t) * kBlockM; };
     auto tile_nkt = [&](int it, int t) {
         const int qt = item_cq(it) * NQ + t;
-        if (qt * kBlockM >= p.N || !head_on(it)) return 0;
+        if (qt * kBlockM >= p.N) return 0;
         return CAUSAL ? (qt + 1 < n_ktiles_all ? qt + 1 : n_ktiles_all) : n_ktiles_all;
     };
     auto item_nkt = [&](int it) {
@@ -225,6 +242,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     const int it = fwd_item(r);
                     if (it >= p.n_items) break;
                     const int bh = item_bh(it), cq = item_cq(it);
+                    const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
                     const int qb = n % QB;
                     const uint32_t uq = static_cast<uint32_t>(n / QB);
                     // the Q buffer is free once both tiles' last S of item n - QB is done
@@ -236,8 +254,8 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     for (int t = 0; t < NQ; ++t) {
                         if (tile_nkt(it, t) == 0) continue;
                         for (int b = 0; b < D / 64; ++b)
-                            tma_load_3d(sb + L::kQ + (qb * NQ + t) * L::kTileBytes + b * 16384, &tm_q,
-                                        bar(L::kQFull + qb), b * 64, tile_q0(cq, t), bh);
+                            tma_load_rows(sb + L::kQ + (qb * NQ + t) * L::kTileBytes + b * 16384, &tm_q,
+                                        bar(L::kQFull + qb), b * 64, tile_q0(cq, t), hh, bb, p.lay.head_inner);
                     }
                     const int n_kt = item_nkt(it);
                     for (int j = 0; j < n_kt; ++j, ++g) {
@@ -254,13 +272,13 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                         if (!withhold) {
                             mbar_arrive_expect_tx(bar(L::kKFull + s), L::kTileBytes);
                             for (int b = 0; b < D / 64; ++b)
-                                tma_load_3d(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
-                                            b * 64, j * kBlockN, bh);
+                                tma_load_rows(sb + L::kK + s * L::kTileBytes + b * 16384, &tm_k, bar(L::kKFull + s),
+                                            b * 64, j * kBlockN, hh, bb, p.lay.head_inner);
                         }
                         mbar_arrive_expect_tx(bar(L::kVFull + s), L::kTileBytes);
                         for (int b = 0; b < D / 64; ++b)
-                            tma_load_3d(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
-                                        b * 64, j * kBlockN, bh);
+                            tma_load_rows(sb + L::kV + s * L::kTileBytes + b * 16384, &tm_v, bar(L::kVFull + s),
+                                        b * 64, j * kBlockN, hh, bb, p.lay.head_inner);
                     }
                 }
                 // Every copy this thread issued must have landed before the CTA
@@ -678,25 +696,26 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     if (row == 0) {
                         ok = mbar_wait(bar(L::kOStaged + t), static_cast<uint32_t>(ne) & 1u, p.status);
                         if (ok) {
+                            const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
                             if (MODE == 2) {
-                                tma_store_3d(&tm_o, stg, 0, q0, bh);
-                                tma_store_3d(&tm_o, stg + 16384, 32, q0, bh);
+                                tma_store_rows(&tm_o, stg, 0, q0, hh, bb, p.lay.head_inner);
+                                tma_store_rows(&tm_o, stg + 16384, 32, q0, hh, bb, p.lay.head_inner);
                             } else {
-                                tma_store_3d(&tm_o, stg, 0, q0, bh);
+                                tma_store_rows(&tm_o, stg, 0, q0, hh, bb, p.lay.head_inner);
                             }
                             bulk_commit();
                         }
                     }
                 } else if (store) {
                     if (MODE == 2) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + rowid * D);
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + p.lay.row(bh, qrow));
 #pragma unroll
                         for (int e = 0; e < D / 4; ++e)
                             dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
                                                  __uint_as_float(ov[4 * e + 2]) * inv_l,
                                                  __uint_as_float(ov[4 * e + 3]) * inv_l);
                     } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + rowid * D);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + p.lay.row(bh, qrow));
 #pragma unroll
                         for (int e = 0; e < D / 8; ++e) {
                             uint4 w;
@@ -760,11 +779,16 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.test_withhold_k = a.test_withhold_k;
     p.shift = a.shift;
     p.rs_in = a.rs_in;
-    p.head_mask = a.head_mask;
-    p.H = a.H > 0 ? a.H : 1;
+    p.H = a.lay.H;
+    p.lay = a.lay;
+    // ~0: every head (H may exceed 64); else a set of heads h < H <= 64
+    const uint64_t all = p.H >= 64 ? ~0ull : ((1ull << p.H) - 1ull);
+    p.head_mask = a.head_mask & all;
+    p.Hon = (a.head_mask == ~0ull) ? p.H : __builtin_popcountll(p.head_mask);
+    p.BHon = a.BH / p.H * p.Hon;
     const int n_qt = (a.N + kBlockM - 1) / kBlockM;
     p.n_cq = (n_qt + NQ - 1) / NQ;
-    p.n_items = a.BH * p.n_cq;
+    p.n_items = p.BHon * p.n_cq;
     // persistent: one CTA per SM (or per item, if fewer)
     const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     dim3 grid(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));

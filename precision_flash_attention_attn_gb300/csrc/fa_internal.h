@@ -10,6 +10,24 @@ namespace fa {
 constexpr int kBlockM = 128;  // query rows per tile (one TMEM lane per row)
 constexpr int kBlockN = 128;  // keys per tile
 
+// Where row n of head bh = b*H + h of a [*, N, d] tensor (q, k, v, o, dO,
+// dq, dk, dv) starts, in elements: b*sB + h*sH + n*sN; the d elements of a
+// row are contiguous.  [B, H, N, d]: sN = d, sH = N*d, sB = H*N*d;
+// [B, N, H, d]: sN = H*d, sH = d, sB = N*H*d.
+// The tensor maps list the dimensions in increasing stride order: (d, N, H,
+// B) for [B, H, N, d] and (d, H, N, B) for [B, N, H, d] (head_inner = 1), so
+// a tile's coordinates are (column, row, head, batch) or (column, head, row,
+// batch).
+struct RowLayout {
+    int H;
+    int head_inner;
+    long long sN, sH, sB;
+    __host__ __device__ size_t row(int bh, int n) const {
+        return static_cast<size_t>(bh / H) * static_cast<size_t>(sB) +
+               static_cast<size_t>(bh % H) * static_cast<size_t>(sH) + static_cast<size_t>(n) * static_cast<size_t>(sN);
+    }
+};
+
 
 struct FwdArgs {
     const CUtensorMap* tm_q;
@@ -33,6 +51,7 @@ struct FwdArgs {
     const int32_t* rs_in; // nullable, statistics variant: tie counts to report
     uint64_t head_mask = ~0ull;  // heads h (bit h, h < 64) computed by this launch; ~0: all
     int H = 0;                   // heads per batch (for head_mask)
+    RowLayout lay;               // q, k, v, o (the maps are built with the same strides)
 };
 
 // Row statistics pre-pass of the stabilised softmax with a tolerance eps:
@@ -45,6 +64,7 @@ struct RowShiftArgs {
     int32_t* rs;    // nullable: [BH, N] near-tie counts
     int BH, N, d, causal, mode;
     float scale, beta, eps;
+    RowLayout lay;  // q, k
 };
 cudaError_t launch_row_shift(const RowShiftArgs& a, cudaStream_t stream);
 
@@ -82,6 +102,7 @@ struct BwdArgs {
     const float* o32 = nullptr;   // per-head modes: FP32 O of the heads in fp32_mask
     uint64_t fp32_mask = 0;       // heads h (bit h) whose delta uses o32 instead of o
     int H = 0;
+    RowLayout lay;                // q, k, v, o, dO, dq, dk, dv (dq_acc is [BH, N, d])
     void* dq;                     // [BH, N, d] BF16
     void* dk;
     void* dv;

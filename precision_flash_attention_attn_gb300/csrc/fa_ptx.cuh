@@ -88,6 +88,39 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 4-D tiles of the [*, N, d] tensors: coordinates (column, row, head, batch),
+// so one map serves the [B, H, N, d] and [B, N, H, d] layouts alike.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+        " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// A tile of rows starting at `row` of head (h, b), in the map's dimension
+// order (see RowLayout: the head may be the inner of the two).
+__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int col, int row,
+                                              int h, int b, int head_inner) {
+    const int c1 = head_inner ? h : row, c2 = head_inner ? row : h;
+    tma_load_4d(dst, map, bar, col, c1, c2, b);
+}
+
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, uint32_t src, int col, int row, int h, int b,
+                                               int head_inner) {
+    const int c1 = head_inner ? h : row, c2 = head_inner ? row : h;
+    tma_store_4d(map, src, col, c1, c2, b);
+}
+
 // Element-wise add of a shared-memory tile into global memory (FP32 add).
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0,
                                                   int c1, int c2) {

@@ -33,17 +33,15 @@ __global__ void __launch_bounds__(128) row_shift_kernel(const RowShiftArgs a) {
     const int r0 = blockIdx.x * 128;
     const int i = r0 + threadIdx.x;
     const bool valid = i < a.N;
-    const size_t head = static_cast<size_t>(bh) * a.N * D;
-
     float q[D];
 #pragma unroll
-    for (int c = 0; c < D; ++c) q[c] = valid ? bf16_load(a.q, head + static_cast<size_t>(i) * D + c) : 0.f;
+    for (int c = 0; c < D; ++c) q[c] = valid ? bf16_load(a.q, a.lay.row(bh, i) + c) : 0.f;
     const int kend = a.causal ? min(a.N, r0 + 128) : a.N;
     auto load_k = [&](int j0) {
         for (int e = threadIdx.x; e < KC * D; e += 128) {
             const int jj = e / D, c = e % D;
             const int j = j0 + jj;
-            sk[jj][c] = (j < kend) ? bf16_load(a.k, head + static_cast<size_t>(j) * D + c) : 0.f;
+            sk[jj][c] = (j < kend) ? bf16_load(a.k, a.lay.row(bh, j) + c) : 0.f;
         }
     };
     auto score = [&](int jj) {

@@ -50,6 +50,10 @@ DELTA_RECOMPUTED_O_FP32 = 1   # delta from O recomputed as P V in FP32 inside th
 DELTA_FROM_DP_P = 2           # delta = rowsum(dP o P), no output read
 _lib.fa_tie_stats_ex.argtypes = [_P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P, _P, _P]
 _lib.fa_delta_error_split.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _P, _P, _P, _P]
+_lib.fa_fwd_layout.argtypes = [_P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _SP, _i, _P]
+_lib.fa_bwd_layout.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _i, _i, _P]
+LAYOUT_BHND = 0   # [B, H, N, d]
+LAYOUT_BNHD = 1   # [B, N, H, d]
 _lib.fa_fwd_heads.argtypes = [_P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _P, _SP, _P]
 _lib.fa_bwd_heads.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _f, _P, _P]
 _lib.fa_device_status.argtypes = [_P, _i]
@@ -61,7 +65,7 @@ _lib.fa_status_string.argtypes = [_i]
 _lib.fa_status_string.restype = ctypes.c_char_p
 for _fn in (_lib.fa_fwd, _lib.fa_bwd, _lib.fa_tie_stats, _lib.fa_device_status, _lib.fa_profile_start,
             _lib.fa_profile_stop, _lib.fa_fwd_ex, _lib.fa_tie_stats_ex, _lib.fa_bwd_ex, _lib.fa_delta_error_split,
-            _lib.fa_fwd_heads, _lib.fa_bwd_heads):
+            _lib.fa_fwd_heads, _lib.fa_bwd_heads, _lib.fa_fwd_layout, _lib.fa_bwd_layout):
     _fn.restype = ctypes.c_int
 
 
@@ -186,6 +190,22 @@ def fa_delta_error_split(q, k, v, o, dO, B, H, N, d, causal, scale, mode, err_on
                                    float(scale), int(mode), _params(beta, eps), _ptr(err_one), _ptr(err_rest),
                                    _ptr(err_out), _stream(stream))
     return _check("fa_delta_error_split", rc) if check else rc
+
+
+def fa_fwd_layout(q, k, v, o, lse, B, H, N, d, causal, scale, mode, layout, beta=None, eps=None, stream=None,
+                  check=True):
+    """fa_fwd_ex with a tensor layout (LAYOUT_BHND or LAYOUT_BNHD)."""
+    rc = _lib.fa_fwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(causal), float(scale),
+                            int(mode), _params(beta, eps), int(layout), _stream(stream))
+    return _check("fa_fwd_layout", rc) if check else rc
+
+
+def fa_bwd_layout(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, layout, stream=None,
+                  check=True):
+    """fa_bwd with a tensor layout (LAYOUT_BHND or LAYOUT_BNHD)."""
+    rc = _lib.fa_bwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                            B, H, N, d, int(causal), float(scale), int(mode), int(layout), _stream(stream))
+    return _check("fa_bwd_layout", rc) if check else rc
 
 
 def _head_modes(head_modes):

@@ -20,7 +20,7 @@ def test_library_exports_every_declared_symbol():
     assert set(declared) == {"fa_fwd", "fa_bwd", "fa_tie_stats", "fa_device_status", "fa_status_string",
                              "fa_profile_start", "fa_profile_stop", "fa_last_error", "fa_bwd_noalloc",
                              "fa_fwd_ex", "fa_tie_stats_ex", "fa_bwd_ex", "fa_delta_error_split",
-                             "fa_fwd_heads", "fa_bwd_heads"}
+                             "fa_fwd_heads", "fa_bwd_heads", "fa_fwd_layout", "fa_bwd_layout"}
     lib = ctypes.CDLL(fa.library_path())
     for name in declared:
         assert hasattr(lib, name), name
@@ -206,3 +206,11 @@ def test_head_modes_need_their_output_buffer():
 def test_head_modes_at_most_64_heads():
     assert _fwd_heads([0] * 65) == 2
     assert _bwd_heads([2] * 65) == 2
+
+
+@pytest.mark.parametrize("layout", [2, -1])
+def test_unknown_layout_rejected(layout):
+    assert fa.fa_fwd_layout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 1, 0.125, 0, layout, stream=0,
+                            check=False) == 1
+    assert fa.fa_bwd_layout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 1, 0.125, 0,
+                            layout, stream=0, check=False) == 1

@@ -56,3 +56,32 @@ def test_head_modes_match_uniform_calls(fa, other):
         assert torch.equal(dk[:, h], dk_ref) and torch.equal(dv[:, h], dv_ref), h
         rel = ((dq[:, h].float() - dq_ref.float()).norm() / dq_ref.float().norm()).item()
         assert rel < 1e-4, (h, rel)
+
+
+@pytest.mark.parametrize("B,H,N,modes", [(3, 5, 300, [2, 0, 0, 0, 0]), (2, 7, 200, [1, 2, 2, 0, 1, 0, 2]),
+                                         (1, 3, 129, [0, 0, 2])])
+def test_sparse_head_sets(fa, B, H, N, modes):
+    # a launch's item list holds only its own heads: every head of every set
+    # size and position must come out as in the uniform call of its mode
+    import torch
+    from precision_flash_attention_attn_gb300.inputs import CaseSpec, make_custom
+    c = make_custom(CaseSpec("heads", B, H, N, 64, True, 9400 + N + H, plant_frac=0.1, min_plant_row=3))
+    q, k, v, do = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    o16 = torch.full((B, H, N, 64), float("nan"), device="cuda", dtype=torch.bfloat16)
+    o32 = torch.full((B, H, N, 64), float("nan"), device="cuda", dtype=torch.float32)
+    lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+    fa.fa_fwd_heads(q, k, v, o16, o32, lse, B, H, N, 64, True, c.scale, modes)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    fa.fa_bwd_heads(q, k, v, o16, o32, lse, do, dq, dk, dv, B, H, N, 64, True, c.scale, modes)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for m in sorted(set(modes)):
+        o, l = fa.attention_fwd(q, k, v, True, c.scale, m)
+        gq, gk, gv = fa.attention_bwd(q, k, v, o, l, do, True, c.scale, m)
+        torch.cuda.synchronize()
+        for h in (h for h in range(H) if modes[h] == m):
+            got = o32 if m == 2 else o16
+            assert torch.equal(got[:, h], o[:, h]) and torch.equal(lse[:, h], l[:, h]), (m, h)
+            assert torch.equal(dk[:, h], gk[:, h]) and torch.equal(dv[:, h], gv[:, h]), (m, h)
+            rel = ((dq[:, h].float() - gq[:, h].float()).norm() / gq[:, h].float().norm()).item()
+            assert rel < 1e-4, (m, h, rel)
