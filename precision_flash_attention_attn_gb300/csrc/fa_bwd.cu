@@ -104,7 +104,7 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
                 if (sub == 0) lse[u] = p.lse[static_cast<size_t>(bh) * p.N + i];
             } else if (valid[u]) {
                 const size_t row = static_cast<size_t>(bh) * p.N + i;
-                const size_t base = p.lay.row(bh, i) + sub * 8;
+                const size_t base = (p.lay.head_inner ? p.lay.row(bh, i) : row * D) + sub * 8;
                 g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
                 if (O32) {
                     o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
