@@ -133,8 +133,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * Reads q, k, v, o, lse, dO; writes dq, dk, dv (BF16, FP32 accumulation).
  * Allocates a stream-ordered workspace (cudaMallocAsync on `stream`, freed on
  * `stream` before return; FA_ERR_ALLOC if that fails) of Z + R bytes, where
- * Z = 256 + ceil(B*H*ceil(N/128)*16 / 256)*256 + B*H*N*d*4 (grid-barrier
- * words, dQ tile counts, FP32 dQ accumulator; cleared with cudaMemsetAsync)
+ * Z = 256 + B*H*N*d*4 (grid-barrier words, FP32 dQ accumulator; cleared
+ * with cudaMemsetAsync)
  * and R = 2*B*H*ceil(N/128)*128*4 (per-row LSE and delta terms).  The first time a workspace size is seen on a
  * device, the release threshold of the device's current memory pool is raised
  * to at least that size (never lowered), so steady-state calls reuse pool
@@ -341,7 +341,7 @@ int fa_delta_error_split(const void* q, const void* k, const void* v, const void
  * beta on a large repeated maximum; its O is then not finite either),
  * FA_ERR_CUDA if the synchronisation failed, else FA_OK.  reset != 0 clears
  * the recorded status (and, after a timeout, the allocation-free backward's
- * grid-barrier words).
+ * grid-barrier words and accumulator).
  */
 int fa_device_status(fa_stream_t stream, int reset);
 

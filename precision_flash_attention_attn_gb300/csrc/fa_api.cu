@@ -893,7 +893,7 @@ int fa_device_status(fa_stream_t stream, int reset) {
         const int zero = 0;
         if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
         // a launch that gave up may have left the allocation-free backward's
-        // zero region (barrier words, counts, accumulator) dirty
+        // zero region (barrier words, accumulator) dirty
         void* scratch = nullptr;
         {
             std::lock_guard<std::mutex> lk(g_noalloc_mu);
