@@ -65,6 +65,11 @@ struct BwdParams {
 };
 
 constexpr int kBwdThreads = 512;
+// grid barrier words (p.sync): one arrival count per barrier, each on its
+// own 128-byte line, and the count of CTAs past the last barrier
+constexpr int kSyncBar1 = 0;   // phase A -> main
+constexpr int kSyncBar2 = 32;  // main -> phase C
+constexpr int kSyncExit = 64;
 constexpr uint32_t kBarDrained = 1;  // named barrier: the drain warps' reduce-adds have landed (math + drain)
 constexpr uint32_t kBarGo = 2;       // named barrier: phase C may start (math + drain)
 
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     } else {
         prepare_rows<D, false>(p, -1);
     }
-    const bool started = grid_barrier(p.sync, p.status);
+    const bool started = grid_barrier(p.sync + kSyncBar1, p.status);
 
     if (started) {
     if (warp >= L::kDrainWarp0) {
@@ -823,7 +828,8 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     // hand-back is needed.)
     named_sync(kBarDrained, L::kMathThreads + L::kDrainThreads);
     if (threadIdx.x == 0) {
-        const bool drained = grid_arrive_wait(p.sync, p.status);
+        const bool drained = grid_arrive_wait(p.sync + kSyncBar2, p.status);
+        if (drained) grid_exit(p.sync + kSyncBar1, p.sync + kSyncBar2, p.sync + kSyncExit);
         *reinterpret_cast<volatile int*>(smem + L::kFlag) = drained ? 1 : 0;
     }
     named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);

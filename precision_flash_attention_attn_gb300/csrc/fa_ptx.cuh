@@ -353,58 +353,55 @@ __device__ __forceinline__ void fence_async_global() {
 }
 
 // One thread's part of a barrier over every CTA of the grid, which must all
-// be resident at once (the launch is cooperative).  sync[0] counts arrivals
-// (a reduction without return value, so arriving costs no round trip);
-// thread 0 of CTA 0 waits for the count to reach the grid size, resets it and
-// releases everyone by raising the generation number sync[1], which only
-// grows, so the two words stay valid from one launch to the next once zeroed.
-// The caller first synchronises its CTA (so that this thread's arrival stands
-// for every thread's earlier writes) and afterwards releases the CTA's
-// threads; global writes made before the barrier are then visible after it,
-// to either proxy.  Bounded: a thread that waits longer than kWaitLimitNs
-// records a timeout in *status and returns false.
-__device__ __forceinline__ bool grid_arrive_wait(uint32_t* sync, int* status) {
+// be resident at once (the launch is cooperative).  Each barrier of a launch
+// has its own arrival count `cnt` (zero at launch): the thread adds one with a
+// release reduction (no return value, so arriving costs no round trip) and
+// polls the count with acquire loads until it reaches the grid size.  No CTA
+// resets or releases anything on the critical path: the counts are zeroed at
+// the end of the launch (grid_exit).  The caller first synchronises its CTA
+// (so that this thread's arrival stands for every thread's earlier writes)
+// and afterwards releases the CTA's threads; global writes made before the
+// barrier are then visible after it, to either proxy.  Bounded: a thread that
+// waits longer than kWaitLimitNs records a timeout in *status and returns
+// false.
+__device__ __forceinline__ bool grid_arrive_wait(uint32_t* cnt, int* status) {
     bool ok = true;
-    const uint32_t gen = ld_acquire_gpu(sync + 1);
-    __threadfence();
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sync) : "memory");
+    fence_async_global();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
     const unsigned long long t0 = global_ns();
-    if (blockIdx.x == 0) {
-        while (ld_acquire_gpu(sync) != gridDim.x) {
-            if (global_ns() - t0 > kWaitLimitNs) {
-                ok = false;
-                break;
-            }
-        }
-        if (ok) {
-            atomicExch(sync, 0u);
-            __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(sync + 1), "r"(gen + 1u) : "memory");
-        }
-    } else {
-        while (ld_acquire_gpu(sync + 1) == gen) {
-            if (global_ns() - t0 > kWaitLimitNs) {
-                ok = false;
-                break;
-            }
+    while (ld_acquire_gpu(cnt) < gridDim.x) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            break;
         }
     }
     if (!ok && status) atomicOr(status, kDevTimeout);
-    __threadfence();
     fence_async_global();
     return ok;
 }
 
 // Grid barrier taken by every thread of the CTA (see grid_arrive_wait); the
 // verdict is the same for all of them.
-__device__ __forceinline__ bool grid_barrier(uint32_t* sync, int* status) {
+__device__ __forceinline__ bool grid_barrier(uint32_t* cnt, int* status) {
     fence_async_global();
     __syncthreads();
     int ok = 1;
-    if (threadIdx.x == 0) ok = grid_arrive_wait(sync, status) ? 1 : 0;
+    if (threadIdx.x == 0) ok = grid_arrive_wait(cnt, status) ? 1 : 0;
     ok = __syncthreads_and(ok);
     fence_async_global();
     return ok != 0;
+}
+
+// Called once per CTA (one thread) after the launch's last grid barrier has
+// passed: counts the CTAs that are done polling in *exits; the last one
+// zeroes the two barriers' counts and the exit count, which no CTA reads any
+// more, so that they start the next launch at zero.
+__device__ __forceinline__ void grid_exit(uint32_t* cnt_a, uint32_t* cnt_b, uint32_t* exits) {
+    if (atomicAdd(exits, 1u) == gridDim.x - 1) {
+        atomicExch(cnt_a, 0u);
+        atomicExch(cnt_b, 0u);
+        atomicExch(exits, 0u);
+    }
 }
 
 // Named CTA barriers (ids 1..15; id 0 is __syncthreads): `count` threads,
