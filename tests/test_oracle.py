@@ -494,3 +494,40 @@ def test_delta_split_stabilised_tied_row_has_no_unit_part():
     s0 = orc.delta_split(q, k, v, o, g, 0, 0.5, 0)
     assert np.all(s1["one"] == 0.0)
     assert np.all(s0["one"] != 0.0)
+
+
+# Running maximum M and count C across key tiles, worked by hand.  One query
+# e0 against keys whose first component is the chosen score (every value
+# BF16-exact), scale 1, two keys per tile, all keys visible.  Per tile: M and
+# C update with the tile's max; the shift m = f(M, C) is re-taken; a changed
+# m rescales the accumulator and restarts the count of keys whose final
+# weight is 1; then Pbar = exp(s - m).  (p_one0, p_one1) per mode:
+#   [1, .5 | 1, 2 | 2, 0]   baseline: tile 1 feeds key 0 as 1, tile 2 raises
+#       M to 2 (key 3 fed as 1), tile 3 ties it (key 4 fed as 1): (3, 2);
+#       stabilised: tiles 1, 2 as baseline (C = 1), tile 3 makes C = 2 so
+#       m = 2*2 = 4, a rescale, and no unit entry: (2, 0).
+#   [1, 1 | 2, .5 | 2, 0]   baseline: (4, 2).  stabilised: tile 1 has C = 2,
+#       m = 2; tile 2 raises M to 2 with C = 1, m = 2 unchanged (no rescale),
+#       key 2 fed as 1; tile 3: C = 2, m = 4, rescale: (1, 0).
+#   [-1, -3 | -1, -2]        baseline: (2, 2).  stabilised: tile 2 makes
+#       C = 2 with M < 0, so m = 0 and the first key's 1 is rescaled: (1, 0).
+@pytest.mark.parametrize("scores,base,stab", [
+    ([1.0, 0.5, 1.0, 2.0, 2.0, 0.0], (3, 2), (2, 0)),
+    ([1.0, 1.0, 2.0, 0.5, 2.0, 0.0], (4, 2), (1, 0)),
+    ([-1.0, -3.0, -1.0, -2.0], (2, 2), (1, 0)),
+])
+def test_emulation_multi_tile_counts_hand_worked(scores, base, stab):
+    N, d = len(scores), 4
+    q = np.zeros((1, N, d), np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, N, d), np.float32)
+    k[0, :, 0] = scores
+    v = np.random.default_rng(11).standard_normal((1, N, d)).astype(np.float32)
+    ex = orc.fwd(q, k, v, False, 1.0, 0)
+    for mode, want in ((0, base), (1, stab)):
+        em = orc.fwd_emul(q, k, v, False, 1.0, mode, beta=2.0, block_n=2)
+        assert np.all(em["p_one0"] == want[0]), (mode, em["p_one0"])
+        assert np.all(em["p_one1"] == want[1]), (mode, em["p_one1"])
+        # the shift is exact in real arithmetic: LSE and O stay the exact ones
+        np.testing.assert_allclose(em["lse"], ex["lse"], rtol=0, atol=1e-6)
+        assert np.abs(em["o"] - ex["o"]).max() <= 2.0 ** -8 * np.abs(v).max() + 2.0 ** -9 * np.abs(ex["o"]).max()
