@@ -12,6 +12,9 @@ reports over the rows with a planted tie whose exact tie count is > 1:
   * pv_err:       mean and standard error of sum_c (O - O_ref);
   * delta_err:    mean and standard error of sum_c dO (O - O_ref), the error
                   of the backward's delta (section 3.4.4, "Cause 2");
+  * delta_split:  the same error split (fa_delta_error_split) into the keys
+                  whose BF16 probability is 1, the other keys, and the
+                  output's rounding, mean and standard error of each;
   * nonfinite_rows: rows whose output is not finite (a large beta underflows
                   every Pbar of a row with a large repeated maximum), which the
                   means leave out.
@@ -73,28 +76,34 @@ def main(argv=None) -> int:
         po = torch.empty((2, B, H, N), device="cuda", dtype=torch.int32)
         fa.fa_tie_stats_ex(q, k, v, o, B, H, N, d, c.causal, c.scale, mode, tc, pe, po, dO=do, delta_err=de,
                            beta=beta)
+        split = fa.delta_error_split(q, k, v, o, do, c.causal, c.scale, mode, beta=beta)
         finite = torch.isfinite(o.float()).all(-1)
         status = fa.fa_device_status()
         if status not in (0, 6):            # FA_ERR_NONFINITE is counted below, not an error
             raise RuntimeError(f"device status {fa.fa_status_string(status)}")
         return (tc.cpu().numpy().reshape(-1), pe.cpu().numpy().reshape(-1).astype(np.float64),
                 po.cpu().numpy().reshape(2, -1), de.cpu().numpy().reshape(-1).astype(np.float64),
-                finite.cpu().numpy().reshape(-1))
+                finite.cpu().numpy().reshape(-1),
+                [t.cpu().numpy().reshape(-1).astype(np.float64) for t in split])
 
     tc0 = run(0, None)[0]
     rows = np.flatnonzero(c.planted.reshape(-1) & (tc0 > 1))
     settings = [("baseline", 0, None)] + [(f"stabilised beta={b:g}", 1, b) for b in betas]
     for name, mode, beta in settings:
-        _, pe, po, de, finite = run(mode, beta)
+        _, pe, po, de, finite, split = run(mode, beta)
         ok = rows[finite[rows]]
         pv_m, pv_se = _mean_se(pe[ok])
         de_m, de_se = _mean_se(de[ok])
+        parts = {}
+        for name_, arr in zip(("one", "rest", "out"), split):
+            m_, se_ = _mean_se(arr[ok])
+            parts[name_] = {"mean": m_, "se": se_}
         print(json.dumps({
             "workload": args.workload + (" (negative-mean V)" if args.neg_v else ""), "setting": name,
             "tied_rows": int(rows.size),
             "p_one0_rows": float((po[0][rows] > 0).mean()) if rows.size else None,
             "p_one1_mean": float(po[1][rows].mean()) if rows.size else None,
-            "pv_err": {"mean": pv_m, "se": pv_se}, "delta_err": {"mean": de_m, "se": de_se},
+            "pv_err": {"mean": pv_m, "se": pv_se}, "delta_err": {"mean": de_m, "se": de_se}, "delta_split": parts,
             "nonfinite_rows": int((~finite).sum()), "nonfinite_tied_rows": int(rows.size - ok.size),
         }), flush=True)
     return 0

@@ -189,6 +189,11 @@ def test_beta_sweep_runs_on_tiny(fa, capsys):
     for ln in lines[1:]:
         assert ln["p_one1_mean"] < lines[0]["p_one1_mean"]
         assert ln["nonfinite_rows"] == 0
+    # the delta error's three parts add up to it (row by row, so in the mean)
+    for ln in lines:
+        sp = ln["delta_split"]
+        total = sp["one"]["mean"] + sp["rest"]["mean"] + sp["out"]["mean"]
+        assert abs(total - ln["delta_err"]["mean"]) <= 1e-5, (ln["setting"], total, ln["delta_err"])
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
