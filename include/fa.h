@@ -133,16 +133,15 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * Reads q, k, v, o, lse, dO; writes dq, dk, dv (BF16, FP32 accumulation).
  * Allocates a stream-ordered workspace (cudaMallocAsync on `stream`, freed on
  * `stream` before return; FA_ERR_ALLOC if that fails) of Z + R bytes, where
- * Z = 256 + B*H*N*d*4 (grid-barrier words, FP32 dQ accumulator; cleared
- * with cudaMemsetAsync)
- * and R = 2*B*H*ceil(N/128)*128*4 (per-row LSE and delta terms).  The first time a workspace size is seen on a
- * device, the release threshold of the device's current memory pool is raised
- * to at least that size (never lowered), so steady-state calls reuse pool
- * memory instead of returning it to the OS at every synchronisation.
- * The kernel is a persistent, cooperative launch of at most one CTA per SM
- * whose CTAs synchronise across the grid (a bounded wait, FA_ERR_TIMEOUT if
- * it runs out); it must be able to have all its CTAs resident at once, which
- * fails to launch (FA_ERR_CUDA) under an SM partition smaller than the grid.
+ * Z = B*H*N*d*4 (the FP32 dQ accumulator, cleared by the first kernel)
+ * and R = 2*B*H*ceil(N/128)*128*4 (per-row LSE and delta terms).  The first
+ * time a workspace size is seen on a device, the release threshold of the
+ * device's current memory pool is raised to at least that size (never
+ * lowered), so steady-state calls reuse pool memory instead of returning it
+ * to the OS at every synchronisation.  Three kernels run in order on
+ * `stream`: the per-row terms, the persistent main kernel (at most one CTA
+ * per SM; every wait bounded, FA_ERR_TIMEOUT through fa_device_status if one
+ * runs out), and the conversion of dQ to BF16.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dO, void* dq, void* dk, void* dv,
@@ -341,7 +340,7 @@ int fa_delta_error_split(const void* q, const void* k, const void* v, const void
  * beta on a large repeated maximum; its O is then not finite either),
  * FA_ERR_CUDA if the synchronisation failed, else FA_OK.  reset != 0 clears
  * the recorded status (and, after a timeout, the allocation-free backward's
- * grid-barrier words and accumulator).
+ * accumulator).
  */
 int fa_device_status(fa_stream_t stream, int reset);
 
@@ -364,10 +363,9 @@ int fa_device_status(fa_stream_t stream, int reset);
 enum {
     FA_KERNEL_FWD = 0,       /* forward (modes 0-2) */
     FA_KERNEL_FWD_STATS = 1, /* forward replay writing tie counts */
-    FA_KERNEL_BWD_PRE = 2,   /* reserved: no longer launched (phase A of FA_KERNEL_BWD_MAIN) */
-    FA_KERNEL_BWD_MAIN = 3,  /* the backward: delta and LSE*log2(e) per row, the
-                                five-MMA main loop, FP32 dQ accumulator -> BF16 */
-    FA_KERNEL_DQ_CONVERT = 4,/* reserved: no longer launched (phase C of FA_KERNEL_BWD_MAIN) */
+    FA_KERNEL_BWD_PRE = 2,   /* backward, first kernel: delta and LSE*log2(e) per row */
+    FA_KERNEL_BWD_MAIN = 3,  /* backward, main kernel: the five-MMA loop */
+    FA_KERNEL_DQ_CONVERT = 4,/* backward, last kernel: FP32 dQ accumulator -> BF16 */
     FA_KERNEL_PV_ERR = 5,    /* CUDA-core reference for pv_err */
     FA_KERNEL_COUNT = 6,
     FA_PROFILE_MAX_LAUNCHES = 65536

@@ -216,17 +216,16 @@ int launch_row_pass(const void* q, const void* k, int BH, int N, int d, int caus
 float log2e_times(float scale) { return static_cast<float>(static_cast<double>(scale) * 1.4426950408889634); }
 
 // Backward workspace, two regions:
-//   zero region  [grid barrier words, 256 B][FP32 dQ accumulator BH*N*d]:
-//                must be zero when the kernel starts;
+//   zero region  [FP32 dQ accumulator BH*N*d]: zero when the main kernel
+//                starts; a fresh workspace is cleared by the pre kernel, the
+//                allocation-free one is left zeroed by the previous call's
+//                conversion;
 //   row region   [-LSE*log2e BH*Npad][-alpha*delta BH*Npad]: written by the
-//                kernel itself.
-// Every part starts on a 256-byte boundary (BH*N*d*4 and BH*Npad*4 are
-// multiples of 256).
-constexpr size_t kSyncBytes = 256;
-
+//                pre kernel.
+// Both start on a 256-byte boundary (BH*N*d*4 is a multiple of 256).
 struct BwdSizes {
     size_t acc, rows;  // accumulator, one of the two row arrays
-    size_t zero_bytes() const { return kSyncBytes + acc; }
+    size_t zero_bytes() const { return acc; }
     size_t row_bytes() const { return 2 * rows; }
 };
 
@@ -244,9 +243,11 @@ bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o,
            aligned16(dq) && aligned16(dk) && aligned16(dv);
 }
 
-// Enqueue the backward kernel.  `zero` is the zero region (bwd_sizes layout,
-// all zero), `rows` the row region.  clean = 1 asks the kernel to leave the
-// zero region at zero again.  Arguments are already validated.
+// Enqueue the backward kernels.  `zero` is the zero region (bwd_sizes
+// layout), `rows` the row region.  clean = 1: the zero region is already zero
+// and is to be left at zero again (the allocation-free scratch); clean = 0:
+// a fresh workspace, which the pre kernel clears.  Arguments are already
+// validated.
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
                     const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0,
@@ -255,8 +256,7 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     const fa::RowLayout lay = layout_of(layout, H, N, d);
     const int Npad = (N + fa::kBlockM - 1) / fa::kBlockM * fa::kBlockM;
     char* zb = static_cast<char*>(zero);
-    uint32_t* sync = reinterpret_cast<uint32_t*>(zb);
-    float* dq_acc = reinterpret_cast<float*>(zb + kSyncBytes);
+    float* dq_acc = reinterpret_cast<float*>(zb);
     float* lse2 = static_cast<float*>(rows);
     float* delta = lse2 + static_cast<size_t>(BH) * Npad;
     CUtensorMap mq, mk, mv, mdo, macc, mdk, mdv;
@@ -282,7 +282,7 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     a.dq_acc = dq_acc;
     a.lse2 = lse2;
     a.delta = delta;
-    a.sync = sync;
+    a.zero_acc = clean ? 0 : 1;  // a fresh workspace is cleared by the pre kernel
     a.clean = clean;
     a.delta_given = delta_given;
     a.o32 = o32;
@@ -520,9 +520,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
         cudaGetLastError();
         return FA_ERR_ALLOC;
     }
-    // fresh memory: the barrier words, counts and accumulator start at zero
-    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
-    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
                              static_cast<char*>(ws) + z.zero_bytes(), 0, st);
@@ -553,8 +550,6 @@ int fa_bwd_layout(const void* q, const void* k, const void* v, const void* o, co
         cudaGetLastError();
         return FA_ERR_ALLOC;
     }
-    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
-    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
                              static_cast<char*>(ws) + z.zero_bytes(), 0, st, 0, nullptr, 0, layout);
@@ -589,8 +584,6 @@ int fa_bwd_heads(const void* q, const void* k, const void* v, const void* o_bf16
         cudaGetLastError();
         return FA_ERR_ALLOC;
     }
-    cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
-    if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
     // delta of each head from its own stored output: o_fp32 for the heads in
     // mode 2, o_bf16 for the others (a head's o is never read otherwise)
     const void* o_any = (mask[0] | mask[1]) ? o_bf16 : static_cast<const void*>(o_fp32);
@@ -638,8 +631,6 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
             cudaGetLastError();
             return FA_ERR_ALLOC;
         }
-        cudaError_t me = cudaMemsetAsync(ws, 0, z.zero_bytes(), st);
-        if (me != cudaSuccess) rc = cuda_fail("cudaMemsetAsync(workspace)", me);
         float* rows = reinterpret_cast<float*>(static_cast<char*>(ws) + z.zero_bytes());
         if (rc == FA_OK) {
             fa::DeltaPdpArgs pa{};
@@ -893,7 +884,7 @@ int fa_device_status(fa_stream_t stream, int reset) {
         const int zero = 0;
         if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
         // a launch that gave up may have left the allocation-free backward's
-        // zero region (barrier words, accumulator) dirty
+        // zero region (the accumulator) dirty
         void* scratch = nullptr;
         {
             std::lock_guard<std::mutex> lk(g_noalloc_mu);

@@ -9,29 +9,32 @@
 //   dS    = alpha * P o (dP - delta)
 //   dQ    = dS K,   dK = dS^T Q,   dV = P^T dO   (dK, dV: textbook gradients)
 //
-// One persistent kernel, one CTA per SM (the launch is cooperative: all CTAs
-// are resident at once):
-//   A  every thread: -LSE*log2(e) and -alpha*delta per row into padded
-//      workspaces (delta from the stored O of the mode), then a grid barrier.
-//   B  work items (batch*head, 128-key tile); K and V stay in shared memory
-//      while the CTA walks the 128-query tiles (causal: only tiles at or below
-//      the diagonal).  Per query tile, five tcgen05 MMAs:
-//        S^T  = K Q^T      (TMEM, FP32)
-//        dP^T = V dO^T     (TMEM, FP32)
-//        dV  += P^T dO     (TMEM accumulator)
-//        dK  += dS^T Q     (TMEM accumulator)
-//        dQ_t = dS K       (TMEM), added to the FP32 accumulator with TMA
-//                          reduce-add
-//      Warp roles: two math warpgroups (warps 0-3: query columns 0-63 of the
-//      tile, warps 4-7: columns 64-127; thread t of a warpgroup owns key row
-//      t) recompute P^T and dS^T; a drain warpgroup (warps 8-11, one TMEM lane
-//      quarter each) moves each dQ tile from TMEM into the reduce-add and each
-//      item's dK and dV from TMEM to HBM (TMA stores), off the math chain;
-//      warp 12 issues TMA loads; warp 13 issues the MMAs.  The next tile's S^T
-//      and dP^T are issued ahead of the current tile's dK/dQ products.
-//   C  once every CTA's reduce-adds have landed (a grid barrier), the math
-//      warps convert the FP32 dQ accumulator to BF16 (and, when asked, write
-//      zeros back, leaving the accumulator ready for the next call).
+// Three kernels, each launched with programmatic dependent launch so that it
+// is scheduled while its predecessor finishes (its griddepcontrol.wait still
+// waits for the whole predecessor):
+//   pre      -LSE*log2(e) and -alpha*delta per row into padded workspaces
+//            (delta from the stored O of the mode); on a fresh workspace the
+//            same launch clears the FP32 dQ accumulator.
+//   main     persistent, one CTA per SM: work items (batch*head, 128-key
+//            tile); K and V stay in shared memory while the CTA walks the
+//            128-query tiles (causal: only tiles at or below the diagonal).
+//            Per query tile, five tcgen05 MMAs:
+//              S^T  = K Q^T      (TMEM, FP32)
+//              dP^T = V dO^T     (TMEM, FP32)
+//              dV  += P^T dO     (TMEM accumulator)
+//              dK  += dS^T Q     (TMEM accumulator)
+//              dQ_t = dS K       (TMEM), added to the FP32 accumulator with
+//                                TMA reduce-add
+//            Warp roles: two math warpgroups (warps 0-3: query columns 0-63
+//            of the tile, warps 4-7: columns 64-127; thread t of a warpgroup
+//            owns key row t) recompute P^T and dS^T; a drain warpgroup (warps
+//            8-11, one TMEM lane quarter each) moves each dQ tile from TMEM
+//            into the reduce-add and each item's dK and dV from TMEM to HBM
+//            (TMA stores), off the math chain; warp 12 issues TMA loads; warp
+//            13 issues the MMAs.  The next tile's S^T and dP^T are issued
+//            ahead of the current tile's dK/dQ products.
+//   convert  the FP32 dQ accumulator to BF16 (and, when asked, zeros written
+//            back, leaving the accumulator ready for the next call).
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -50,9 +53,9 @@ struct BwdParams {
     void* dq;             // [BH, N, d] BF16 output
     float* lse2;          // [BH, Npad]: -LSE*log2(e), -inf on padded rows
     float* delta;         // [BH, Npad]: -alpha*rowsum(dO o O), 0 on padded rows
-    uint32_t* sync;       // grid barrier words (zero before the first launch)
     int clean;            // 1: leave the accumulator and the barrier words at zero afterwards
-    int delta_given;      // 1: delta already holds -alpha*rowsum(dP o P); phase A forms lse2 only
+    int delta_given;      // 1: delta already holds -alpha*rowsum(dP o P); pre forms lse2 only
+    int zero_acc;         // 1: pre also clears the dQ accumulator (a fresh workspace)
     const float* o32;     // per-head modes: FP32 O of the heads in fp32_mask (o holds the others)
     uint64_t fp32_mask;
     int H;
@@ -65,59 +68,74 @@ struct BwdParams {
 };
 
 constexpr int kBwdThreads = 512;
-// grid barrier words (p.sync): one arrival count per barrier, each on its
-// own 128-byte line, and the count of CTAs past the last barrier
-constexpr int kSyncBar1 = 0;   // phase A -> main
-constexpr int kSyncBar2 = 32;  // main -> phase C
-constexpr int kSyncExit = 64;
-constexpr uint32_t kBarDrained = 1;  // named barrier: the drain warps' reduce-adds have landed (math + drain)
-constexpr uint32_t kBarGo = 2;       // named barrier: phase C may start (math + drain)
+constexpr int kAuxThreads = 256;   // pre and convert kernels
+constexpr int kAuxBlocksPerSM = 8;
 
-// ------------------------------------------------------------- phase A ----
-// D/8 threads per row, 8 elements (16 bytes of dO) each; each thread takes
-// kUnroll rows, a grid stride apart, per step, and every load of a step (dO,
-// O and the LSE) is issued before any is used, so a step costs one memory
-// round trip.  O32: O is FP32 (mode 2).  sel < 0: every row; sel = 0 / 1:
-// only the rows of heads outside / inside fp32_mask (per-head modes), whose
-// O is read from o (BF16) / o32 (FP32).
+// ------------------------------------------------------------------ pre ----
+// D/8 threads per row, 8 elements (16 bytes of dO) each; rows padded to Npad.
+// Each warp takes kUnroll groups of rows at once, every load of a group (dO,
+// O and the LSE) issued before any is used, so that enough loads are in
+// flight to keep HBM busy.  O32: O is FP32 (mode 2).  sel < 0: every row;
+// sel = 0 / 1: only the rows of heads outside / inside fp32_mask (per-head
+// modes), whose O is read from o (BF16) / o32 (FP32).  With zero_acc the
+// second half of the blocks clears the dQ accumulator meanwhile.
 template <int D, bool O32>
-__device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
+__global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdParams p, int sel) {
+    constexpr int TPR = D / 8;       // threads per row
+    constexpr int RPW = 32 / TPR;    // rows per warp and group
+    constexpr int kUnroll = O32 ? 3 : 4;
+    // the next kernel may be scheduled now; it waits for this one to finish
+    griddep_launch_dependents();
+    // the previous kernel (the forward writing O and the LSE, or the previous
+    // user of this workspace's memory) must be done
+    griddep_wait();
+    const int row_blocks = p.zero_acc ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+    if (static_cast<int>(blockIdx.x) >= row_blocks) {
+        const size_t n4 = static_cast<size_t>(p.BH) * p.N * D / 4;
+        float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+        const size_t nthr = static_cast<size_t>(gridDim.x - row_blocks) * blockDim.x;
+        const size_t tid = static_cast<size_t>(blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
+        for (size_t e = tid; e < n4; e += 4 * nthr) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e + u * nthr < n4) acc4[e + u * nthr] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
+    }
     const void* obase = (sel == 1) ? static_cast<const void*>(p.o32) : p.o;
-    constexpr int TPR = D / 8;                  // threads per row
-    constexpr int RPC = kBwdThreads / TPR;      // rows per CTA and step
-    constexpr int kUnroll = O32 ? 5 : 7;
-    const int tid = threadIdx.x;
-    const int sub = tid % TPR;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % TPR;
     // rows < 2^31 (BH * Npad * d is checked against it), so 32-bit index math
     const int rows = p.BH * p.Npad;
-    const int stride = static_cast<int>(gridDim.x) * RPC;
+    const int nwarps = row_blocks * (blockDim.x >> 5);
+    const int gw = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
-    for (int r0 = static_cast<int>(blockIdx.x) * RPC + tid / TPR; r0 < rows; r0 += kUnroll * stride) {
+    for (int r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
         uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
         float lse[kUnroll];
         bool valid[kUnroll], chosen[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int r = r0 + u * stride;
+            const int r = r0 + u * RPW + lane / TPR;
             const int bh = r / p.Npad;
             const int i = r - bh * p.Npad;
             chosen[u] = r < rows && (sel < 0 || static_cast<int>((p.fp32_mask >> (bh % p.H)) & 1ull) == sel);
             valid[u] = chosen[u] && i < p.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
             lse[u] = 0.f;
-            if (valid[u] && p.delta_given) {
-                if (sub == 0) lse[u] = p.lse[static_cast<size_t>(bh) * p.N + i];
-            } else if (valid[u]) {
+            if (valid[u]) {
                 const size_t row = static_cast<size_t>(bh) * p.N + i;
-                const size_t base = (p.lay.head_inner ? p.lay.row(bh, i) : row * D) + sub * 8;
-                g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
-                if (O32) {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
-                    o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base + 4);
-                } else {
-                    o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(obase) + base);
-                }
                 if (sub == 0) lse[u] = p.lse[row];
+                if (!p.delta_given) {
+                    const size_t base = (p.lay.head_inner ? p.lay.row(bh, i) : row * D) + sub * 8;
+                    g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
+                    if (O32) {
+                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
+                        o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base + 4);
+                    } else {
+                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(obase) + base);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -141,9 +159,9 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
             }
 #pragma unroll
             for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            const int r = r0 + u * stride;
+            const int r = r0 + u * RPW + lane / TPR;
             if (sub == 0 && chosen[u]) {
-                // stored pre-negated / pre-scaled for the main phase's FMAs:
+                // stored pre-negated / pre-scaled for the main kernel's FMAs:
                 //   P  = exp2(s * alpha*log2e + lse2),  lse2 = -LSE*log2e
                 //   dS = P * (alpha * dP + delta),      delta = -alpha * rowsum(dO o O)
                 if (!p.delta_given) p.delta[r] = valid[u] ? -p.scale * acc : 0.f;
@@ -154,28 +172,29 @@ __device__ __forceinline__ void prepare_rows(const BwdParams& p, int sel) {
     }
 }
 
-// ------------------------------------------------------------- phase C ----
-// dQ accumulator (FP32) -> BF16 by threads 0..nthreads_cta-1 of every CTA,
-// eight elements per thread and step, four steps' loads in flight; with
-// `clean` the accumulator is zeroed as it is read.  The loads bypass L1: the
-// accumulator was written by other SMs' reduce-adds during this launch.
+// -------------------------------------------------------------- convert ----
+// dQ accumulator (FP32) -> BF16 in the caller's layout, eight elements per
+// thread and step, four steps' loads in flight; with `clean` the accumulator
+// is zeroed as it is read.
 template <int D>
-__device__ __forceinline__ void convert_dq(const BwdParams& p, int nthreads_cta) {
+__global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const BwdParams p) {
     constexpr int kChunks = D / 8;  // eight-element chunks per row
+    griddep_launch_dependents();
+    griddep_wait();  // every reduce-add of the main kernel has landed
     float4* acc = reinterpret_cast<float4*>(p.dq_acc);
     uint4* dq = reinterpret_cast<uint4*>(p.dq);
     // BH * Npad * d < 2^31 (checked on the host): 32-bit chunk indices
     const int n8 = p.BH * p.N * kChunks;
-    const int nthr = static_cast<int>(gridDim.x) * nthreads_cta;
-    const int tid = static_cast<int>(blockIdx.x) * nthreads_cta + static_cast<int>(threadIdx.x);
+    const int nthr = static_cast<int>(gridDim.x * blockDim.x);
+    const int tid = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
     for (int e0 = tid; e0 < n8; e0 += 4 * nthr) {
         float4 x[4], y[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int e = e0 + u * nthr;
             if (e < n8) {
-                x[u] = __ldcg(acc + 2 * static_cast<size_t>(e));
-                y[u] = __ldcg(acc + 2 * static_cast<size_t>(e) + 1);
+                x[u] = acc[2 * static_cast<size_t>(e)];
+                y[u] = acc[2 * static_cast<size_t>(e) + 1];
             }
         }
 #pragma unroll
@@ -247,7 +266,6 @@ struct BwdLayout {
     static constexpr int kDrain = kAccFree + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
-    static constexpr int kFlag = kTmemSlot + 8;   // phase C go-ahead (the grid barrier's verdict)
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static_assert(kAlloc <= 232448, "shared memory budget");
@@ -337,20 +355,12 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-    // Phase A.  Nothing above reads or writes global memory, so under
-    // programmatic dependent launch all of it overlaps the previous kernel.
+    // Nothing above reads or writes global memory, so under programmatic
+    // dependent launch all of it overlaps the previous kernel (pre); the
+    // next one (convert) may be scheduled as this grid's CTAs leave.
     griddep_wait();
-    if (p.fp32_mask != 0) {  // per-head modes: each head's delta from its own stored O
-        prepare_rows<D, false>(p, 0);
-        prepare_rows<D, true>(p, 1);
-    } else if (p.mode == 2) {
-        prepare_rows<D, true>(p, -1);
-    } else {
-        prepare_rows<D, false>(p, -1);
-    }
-    const bool started = grid_barrier(p.sync + kSyncBar1, p.status);
+    griddep_launch_dependents();
 
-    if (started) {
     if (warp >= L::kDrainWarp0) {
     regs_dec<L::kRegsOther>();
     if (warp == L::kProducerWarp) {
@@ -663,20 +673,10 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                 }
             }
         }
-        // every reduce-add has landed (not only read its staging buffer)
-        // before the grid barrier that precedes phase C's reads
-        if (lane == 0) {
-            bulk_wait0();
-            fence_async_global();
-            __threadfence();
-        }
+        // every reduce-add and store has landed (not only read its staging
+        // buffer) before the CTA exits
+        if (lane == 0) bulk_wait0();
         __syncwarp();
-        named_arrive(kBarDrained, L::kMathThreads + L::kDrainThreads);
-        // phase C: these warps convert alongside the math warps
-        named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);
-        fence_async_global();
-        if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
-            convert_dq<D>(p, L::kMathThreads + L::kDrainThreads);
     }
     } else {
     regs_inc<L::kRegsMath>();
@@ -821,24 +821,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             }
         }
     }
-    // ------------------------------------------------------------ phase C
-    // The math and drain warps (threads 0-383) convert the dQ accumulator
-    // once the drain warps of every CTA have seen their reduce-adds land.
-    // (Each in its own branch, within its register budget: no register
-    // hand-back is needed.)
-    named_sync(kBarDrained, L::kMathThreads + L::kDrainThreads);
-    if (threadIdx.x == 0) {
-        const bool drained = grid_arrive_wait(p.sync + kSyncBar2, p.status);
-        if (drained) grid_exit(p.sync + kSyncBar1, p.sync + kSyncBar2, p.sync + kSyncExit);
-        *reinterpret_cast<volatile int*>(smem + L::kFlag) = drained ? 1 : 0;
     }
-    named_sync(kBarGo, L::kMathThreads + L::kDrainThreads);
-    fence_async_global();
-    griddep_launch_dependents();
-    if (*reinterpret_cast<volatile int*>(smem + L::kFlag))
-        convert_dq<D>(p, L::kMathThreads + L::kDrainThreads);
-    }
-    }  // started
 
     tc_fence_before();
     __syncthreads();
@@ -848,16 +831,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     }
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
-    using L = BwdLayout<D>;
-    auto kern = bwd_kernel<D, CAUSAL>;
-    static unsigned smem_set = 0;  // devices on which this instantiation's limit is raised
-    cudaError_t e = smem_limit_once(kern, L::kAlloc, &smem_set);
-    if (e != cudaSuccess) {
-        set_error("bwd_main cudaFuncSetAttribute", e);
-        return e;
-    }
+BwdParams make_params(const BwdArgs& a) {
     BwdParams p;
     p.o = a.o;
     p.lse = a.lse;
@@ -866,9 +840,9 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.dq = a.dq;
     p.lse2 = a.lse2;
     p.delta = a.delta;
-    p.sync = a.sync;
     p.clean = a.clean;
     p.delta_given = a.delta_given;
+    p.zero_acc = a.zero_acc;
     p.o32 = a.o32;
     p.fp32_mask = a.fp32_mask;
     p.H = a.lay.H;
@@ -882,26 +856,66 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     p.scale = a.scale;
     p.scale_log2 = a.scale_log2;
     p.status = a.status;
-    // persistent: one CTA per SM (or per item, if fewer), all resident at once
-    // for the grid barriers (cooperative launch); programmatic dependent
-    // launch lets the set-up overlap the previous kernel in the stream
-    const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    return p;
+}
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel in the stream finishes; its griddepcontrol.wait
+// holds it until that kernel is complete.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, int threads, int smem, cudaStream_t stream,
+                       Args... args) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(n_cta > 0 ? n_cta : 1));
-    cfg.blockDim = dim3(L::kThreads);
-    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    prof_begin(3, stream);
-    e = cudaLaunchKernelEx(&cfg, kern, *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
-    prof_end(3, stream);
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
     if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
+}
+
+template <int D>
+cudaError_t launch_pre(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(num_sms * kAuxBlocksPerSM));
+    cudaError_t e = cudaSuccess;
+    prof_begin(2, stream);
+    if (p.fp32_mask != 0) {  // per-head modes: each head's delta from its own stored O
+        BwdParams p1 = p;
+        p1.zero_acc = 0;     // the first launch clears the accumulator
+        e = launch_pdl(bwd_pre_kernel<D, false>, grid, kAuxThreads, 0, stream, p, 0);
+        if (e == cudaSuccess) e = launch_pdl(bwd_pre_kernel<D, true>, grid, kAuxThreads, 0, stream, p1, 1);
+    } else if (p.mode == 2) {
+        e = launch_pdl(bwd_pre_kernel<D, true>, grid, kAuxThreads, 0, stream, p, -1);
+    } else {
+        e = launch_pdl(bwd_pre_kernel<D, false>, grid, kAuxThreads, 0, stream, p, -1);
+    }
+    prof_end(2, stream);
+    if (e != cudaSuccess) set_error("bwd_pre launch", e);
+    return e;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_main(const BwdArgs& a, const BwdParams& p, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    auto kern = bwd_kernel<D, CAUSAL>;
+    static unsigned smem_set = 0;  // devices on which this instantiation's limit is raised
+    cudaError_t e = smem_limit_once(kern, L::kAlloc, &smem_set);
+    if (e != cudaSuccess) {
+        set_error("bwd_main cudaFuncSetAttribute", e);
+        return e;
+    }
+    // persistent: one CTA per SM (or per item, if fewer)
+    const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    prof_begin(3, stream);
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(n_cta > 0 ? n_cta : 1)), L::kThreads, L::kAlloc, stream,
+                   *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
+    prof_end(3, stream);
     if (e != cudaSuccess) {
         cudaFuncAttributes fa_attr{};
         char msg[200];
@@ -916,11 +930,31 @@ cudaError_t launch_main(const BwdArgs& a, cudaStream_t stream) {
     return e;
 }
 
+template <int D>
+cudaError_t launch_convert(const BwdParams& p, int num_sms, cudaStream_t stream) {
+    prof_begin(4, stream);
+    const cudaError_t e = launch_pdl(dq_convert_kernel<D>, dim3(static_cast<unsigned>(num_sms * kAuxBlocksPerSM)),
+                                     kAuxThreads, 0, stream, p);
+    prof_end(4, stream);
+    if (e != cudaSuccess) set_error("dq_convert launch", e);
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-    if (a.d == 64) return a.causal ? launch_main<64, true>(a, stream) : launch_main<64, false>(a, stream);
-    return a.causal ? launch_main<128, true>(a, stream) : launch_main<128, false>(a, stream);
+    const BwdParams p = make_params(a);
+    cudaError_t e;
+    if (a.d == 64) {
+        if ((e = launch_pre<64>(p, a.num_sms, stream)) != cudaSuccess) return e;
+        e = a.causal ? launch_main<64, true>(a, p, stream) : launch_main<64, false>(a, p, stream);
+        if (e != cudaSuccess) return e;
+        return launch_convert<64>(p, a.num_sms, stream);
+    }
+    if ((e = launch_pre<128>(p, a.num_sms, stream)) != cudaSuccess) return e;
+    e = a.causal ? launch_main<128, true>(a, p, stream) : launch_main<128, false>(a, p, stream);
+    if (e != cudaSuccess) return e;
+    return launch_convert<128>(p, a.num_sms, stream);
 }
 
 }  // namespace fa

@@ -96,7 +96,7 @@ struct BwdArgs {
     float* dq_acc;                // FP32 [BH, N, d] workspace
     float* lse2;                  // FP32 [BH, Npad] workspace: LSE * log2(e)
     float* delta;                 // FP32 [BH, Npad] workspace: rowsum(dO o O)
-    uint32_t* sync;               // grid barrier words, zero before the first launch
+    int zero_acc;                 // 1: the pre kernel clears dq_acc (a fresh workspace)
     int clean;                    // 1: leave dq_acc at zero when done
     int delta_given;              // 1: delta is already in place (rowsum(dP o P) pre-pass)
     const float* o32 = nullptr;   // per-head modes: FP32 O of the heads in fp32_mask

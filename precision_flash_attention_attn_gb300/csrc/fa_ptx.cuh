@@ -340,79 +340,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Order this thread's generic-proxy global accesses with async-proxy ones
-// (TMA loads, stores and reductions), in both directions.
-__device__ __forceinline__ void fence_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// One thread's part of a barrier over every CTA of the grid, which must all
-// be resident at once (the launch is cooperative).  Each barrier of a launch
-// has its own arrival count `cnt` (zero at launch): the thread adds one with a
-// release reduction (no return value, so arriving costs no round trip) and
-// polls the count with acquire loads until it reaches the grid size.  No CTA
-// resets or releases anything on the critical path: the counts are zeroed at
-// the end of the launch (grid_exit).  The caller first synchronises its CTA
-// (so that this thread's arrival stands for every thread's earlier writes)
-// and afterwards releases the CTA's threads; global writes made before the
-// barrier are then visible after it, to either proxy.  Bounded: a thread that
-// waits longer than kWaitLimitNs records a timeout in *status and returns
-// false.
-__device__ __forceinline__ bool grid_arrive_wait(uint32_t* cnt, int* status) {
-    bool ok = true;
-    fence_async_global();
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
-    const unsigned long long t0 = global_ns();
-    while (ld_acquire_gpu(cnt) < gridDim.x) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-            ok = false;
-            break;
-        }
-    }
-    if (!ok && status) atomicOr(status, kDevTimeout);
-    fence_async_global();
-    return ok;
-}
-
-// Grid barrier taken by every thread of the CTA (see grid_arrive_wait); the
-// verdict is the same for all of them.
-__device__ __forceinline__ bool grid_barrier(uint32_t* cnt, int* status) {
-    fence_async_global();
-    __syncthreads();
-    int ok = 1;
-    if (threadIdx.x == 0) ok = grid_arrive_wait(cnt, status) ? 1 : 0;
-    ok = __syncthreads_and(ok);
-    fence_async_global();
-    return ok != 0;
-}
-
-// Called once per CTA (one thread) after the launch's last grid barrier has
-// passed: counts the CTAs that are done polling in *exits; the last one
-// zeroes the two barriers' counts and the exit count, which no CTA reads any
-// more, so that they start the next launch at zero.
-__device__ __forceinline__ void grid_exit(uint32_t* cnt_a, uint32_t* cnt_b, uint32_t* exits) {
-    if (atomicAdd(exits, 1u) == gridDim.x - 1) {
-        atomicExch(cnt_a, 0u);
-        atomicExch(cnt_b, 0u);
-        atomicExch(exits, 0u);
-    }
-}
-
-// Named CTA barriers (ids 1..15; id 0 is __syncthreads): `count` threads,
-// a multiple of 32, take part; arrive does not wait.
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ------------------------------------------------------------------ math ----
 
 // Packed pairs of FP32 values (one 64-bit register pair) and the paired FP32
