@@ -131,6 +131,9 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * (BF16 in modes 0/1, FP32 in mode 2), dP = dO V^T, dS = scale * P o (dP -
  * delta), dQ = dS K (sections 3.4.2-3.4.3), dK = dS^T Q, dV = P^T dO.
  * Reads q, k, v, o, lse, dO; writes dq, dk, dv (BF16, FP32 accumulation).
+ * When the previous kernel in `stream` is this library's forward, the first
+ * backward kernel starts reading dO while that forward finishes (o and lse
+ * only after it has): dO must not overlap the forward's outputs.
  * Allocates a stream-ordered workspace (cudaMallocAsync on `stream`, freed on
  * `stream` before return; FA_ERR_ALLOC if that fails) of Z + R bytes, where
  * Z = B*H*N*d*4 (the FP32 dQ accumulator, cleared by the first kernel)

@@ -86,11 +86,10 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdParams p,
     constexpr int kUnroll = O32 ? 3 : 4;
     // the next kernel may be scheduled now; it waits for this one to finish
     griddep_launch_dependents();
-    // the previous kernel (the forward writing O and the LSE, or the previous
-    // user of this workspace's memory) must be done
-    griddep_wait();
     const int row_blocks = p.zero_acc ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
     if (static_cast<int>(blockIdx.x) >= row_blocks) {
+        // the previous user of this workspace's memory must be done
+        griddep_wait();
         const size_t n4 = static_cast<size_t>(p.BH) * p.N * D / 4;
         float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
         const size_t nthr = static_cast<size_t>(gridDim.x - row_blocks) * blockDim.x;
@@ -110,10 +109,14 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdParams p,
     const int nwarps = row_blocks * (blockDim.x >> 5);
     const int gw = static_cast<int>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const float log2e = 1.4426950408889634f;
+    bool waited = false;
     for (int r0 = gw * RPW * kUnroll; r0 < rows; r0 += nwarps * RPW * kUnroll) {
         uint4 g[kUnroll], o[kUnroll], o2[kUnroll];
         float lse[kUnroll];
         bool valid[kUnroll], chosen[kUnroll];
+        size_t rowi[kUnroll], base[kUnroll];
+        // dO is an input of the call, not an output of the previous kernel:
+        // its loads are issued before the wait for that kernel
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int r = r0 + u * RPW + lane / TPR;
@@ -123,17 +126,27 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdParams p,
             valid[u] = chosen[u] && i < p.N;
             g[u] = o[u] = o2[u] = make_uint4(0u, 0u, 0u, 0u);
             lse[u] = 0.f;
+            rowi[u] = static_cast<size_t>(bh) * p.N + i;
+            base[u] = (p.lay.head_inner ? p.lay.row(bh, i) : rowi[u] * D) + sub * 8;
+            if (valid[u] && !p.delta_given)
+                g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base[u]);
+        }
+        // O and the LSE come from the previous kernel (the forward); this
+        // launch's writes below must also follow it
+        if (!waited) {
+            griddep_wait();
+            waited = true;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
             if (valid[u]) {
-                const size_t row = static_cast<size_t>(bh) * p.N + i;
-                if (sub == 0) lse[u] = p.lse[row];
+                if (sub == 0) lse[u] = p.lse[rowi[u]];
                 if (!p.delta_given) {
-                    const size_t base = (p.lay.head_inner ? p.lay.row(bh, i) : row * D) + sub * 8;
-                    g[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + base);
                     if (O32) {
-                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base);
-                        o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base + 4);
+                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base[u]);
+                        o2[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(obase) + base[u] + 4);
                     } else {
-                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(obase) + base);
+                        o[u] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(obase) + base[u]);
                     }
                 }
             }

@@ -224,6 +224,12 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
     // Nothing above reads or writes global memory, so under programmatic
     // dependent launch all of it overlaps the previous kernel in the stream.
     griddep_wait();
+    // The next kernel may be launched now: its CTAs take the SMs this grid's
+    // CTAs leave (the causal items are unequal, so some leave early) and
+    // start on work that does not depend on this grid (the backward's first
+    // kernel loads dO); its griddepcontrol.wait still waits for all of this
+    // grid and its memory operations.
+    griddep_launch_dependents();
 
     if (warp >= kProducerWarp) {
         if (NQ == 2) regs_dec<L::kRegsOther>();
@@ -742,7 +748,6 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
 
     // O's TMA stores complete before the CTA exits
     if (L::kTmaStoreO && !STATS && warp < kProducerWarp && (threadIdx.x & 127) == 0) bulk_wait0();
-    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp0) {
