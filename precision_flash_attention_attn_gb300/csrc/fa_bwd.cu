@@ -370,8 +370,11 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
 
     // Nothing above reads or writes global memory, so under programmatic
     // dependent launch all of it overlaps the previous kernel (pre); the
-    // next one (convert) may be scheduled as this grid's CTAs leave.
-    griddep_wait();
+    // next one (convert) may be scheduled as this grid's CTAs leave.  Every
+    // thread but the producer waits for pre here; the producer first issues
+    // its first tiles of K, V, Q and dO (inputs of the call, which pre does
+    // not write) and waits before the per-row terms that pre writes.
+    if (warp != L::kProducerWarp) griddep_wait();
     griddep_launch_dependents();
 
     if (warp >= L::kDrainWarp0) {
@@ -387,6 +390,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
             bool ok = true;
+            bool waited = false;  // griddepcontrol.wait done (before the first per-row load)
             int g = 0;  // query tiles loaded so far (all items)
             int n = 0;  // items started
             for (int r = 0; ok; ++r, ++n) {
@@ -418,6 +422,10 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                                       hh, bb, p.lay.head_inner);
                     }
                     const size_t roff = static_cast<size_t>(bh) * p.Npad + q0;
+                    if (!waited) {
+                        griddep_wait();
+                        waited = true;
+                    }
                     bulk_load(sb + L::kLse + s * 512, p.lse2 + roff, 512, bar(L::kQFull + s));
                     bulk_load(sb + L::kDelta + s * 512, p.delta + roff, 512, bar(L::kQFull + s));
                 }
