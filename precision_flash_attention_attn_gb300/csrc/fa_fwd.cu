@@ -267,8 +267,14 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     for (int j = 0; j < n_kt; ++j, ++g) {
                         const int s = g % S;
                         const uint32_t u = static_cast<uint32_t>(g / S);
+                        // At the start every CTA asks for its Q tiles and all K/V
+                        // stages at once; the first K tile, which the first S
+                        // needs, then queues behind the rest in DRAM.  The later
+                        // stages are issued once it has landed.
+                        if (g == 1 && !(p.test_withhold_k && blockIdx.x == 0))
+                            ok = mbar_wait(bar(L::kKFull), 0u, p.status);
                         // stage s is free once every tile has released round u-1
-                        if (g >= S)
+                        if (ok && g >= S)
                             for (int t = 0; t < NQ && ok; ++t)
                                 ok = mbar_wait(bar(L::kKVEmpty + t * S + s), (u - 1) & 1u, p.status);
                         if (!ok) break;
