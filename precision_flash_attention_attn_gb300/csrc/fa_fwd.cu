@@ -484,10 +484,11 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     for (int c = 0; c < kBlockN; ++c)
                         if (c > lim) s[c] = -INFINITY;
                 }
-                // row max: 3-input max instructions in 8 independent chains
+                // row max: 3-input max instructions in 8 independent chains;
+                // chain e holds the maximum of the keys c = e (mod 8)
                 float tm;
+                float mx[8];
                 {
-                    float mx[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) mx[e] = fmaxf(s[e], s[8 + e]);
 #pragma unroll
@@ -500,38 +501,26 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     // Only C > 1 matters here.  A tile max equal to the running
                     // max adds at least one tie to the C >= 1 already counted, so
                     // C > 1 follows without a count; only a new running max needs
-                    // the tile's own count.  For 2^-76 <= |tm| <= 2^27 the non-tie
-                    // indicator is one saturated FMA per key: (tm - s) * 2^100 is
-                    // 0 exactly at a tie and at least 1 otherwise, because the
-                    // nearest FP32 value below tm lies at least 2^-100 away and
-                    // tm * 2^100 is exact.  Other maxima take the compare loop.
+                    // to know whether the tile holds it twice.  Two distinct keys
+                    // differ either in c mod 8 or, if not, in c div 8; so the
+                    // tile max occurs at least twice exactly when at least two of
+                    // the mod-8 chain maxima, or two of the maxima of the 16
+                    // blocks of 8 consecutive keys, equal it.
                     const bool newmax = tm > M;
                     const bool same = tm == M;
                     if (__any_sync(0xffffffffu, newmax)) {
-                        int tc;
-                        const float atm = fabsf(tm);
-                        const bool in_range = !newmax || (atm >= 0x1p-76f && atm <= 0x1p27f);
-                        if (__all_sync(0xffffffffu, in_range)) {
-                            const float tb = tm * 0x1p100f;
-                            uint64_t nt2[4] = {0ull, 0ull, 0ull, 0ull};  // non-tie counts, as 4 pairs
+                        int na = 0, nb = 0;
 #pragma unroll
-                            for (int e = 0; e < kBlockN / 2; ++e)
-                                nt2[e & 3] = f2_add(nt2[e & 3], f2_pack(fma_sat(s[2 * e], -0x1p100f, tb),
-                                                                        fma_sat(s[2 * e + 1], -0x1p100f, tb)));
-                            float n0, n1;
-                            f2_unpack(f2_add(f2_add(nt2[0], nt2[1]), f2_add(nt2[2], nt2[3])), n0, n1);
-                            tc = kBlockN - static_cast<int>(n0 + n1);
-                        } else {
-                            int tcs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        for (int e = 0; e < 8; ++e) na += (mx[e] == tm) ? 1 : 0;
 #pragma unroll
-                            for (int c = 0; c < kBlockN; c += 8)
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
-                            tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
+                        for (int b = 0; b < kBlockN / 8; ++b) {
+                            const float* v8 = &s[8 * b];
+                            const float bm = fmax3(fmax3(v8[0], v8[1], v8[2]), fmax3(v8[3], v8[4], v8[5]), fmaxf(v8[6], v8[7]));
+                            nb += (bm == tm) ? 1 : 0;
                         }
                         if (newmax) {
                             M = tm;
-                            C = tc;
+                            C = (na >= 2 || nb >= 2) ? 2 : 1;
                         }
                     }
                     if (same) C = 2;

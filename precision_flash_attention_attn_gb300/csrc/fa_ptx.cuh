@@ -372,13 +372,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     return d;
 }
 
-// a * b + c, rounded once and clamped to [0, 1]
-__device__ __forceinline__ float fma_sat(float a, float b, float c) {
-    float d;
-    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // max of three FP32 values in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
