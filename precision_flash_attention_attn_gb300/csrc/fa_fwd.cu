@@ -129,6 +129,24 @@ struct FwdParams {
 // rounds of gridDim.x: round r visits c on even rounds and gridDim.x-1-c on
 // odd ones, which balances the causal work nearly as well as greedy longest-
 // processing-time scheduling.
+// Whether the maximum tm of a tile of kBlockN scores s[c] occurs at least
+// twice, given mx[e] = max of s[c] over c = e (mod 8).  Two distinct keys
+// differ in c mod 8 or, if not, in c div 8, so it does exactly when two of
+// the mod-8 chain maxima, or two of the maxima of the 16 blocks of 8
+// consecutive keys, equal tm.
+__device__ __forceinline__ bool tile_max_repeats(const float (&s)[kBlockN], const float (&mx)[8], float tm) {
+    int na = 0, nb = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) na += (mx[e] == tm) ? 1 : 0;
+#pragma unroll
+    for (int b = 0; b < kBlockN / 8; ++b) {
+        const float* v8 = &s[8 * b];
+        const float bm = fmax3(fmax3(v8[0], v8[1], v8[2]), fmax3(v8[3], v8[4], v8[5]), fmaxf(v8[6], v8[7]));
+        nb += (bm == tm) ? 1 : 0;
+    }
+    return na >= 2 || nb >= 2;
+}
+
 // Position of the k-th (from 0) set bit of m; m has more than k set bits.
 __device__ __forceinline__ int nth_set_bit(uint64_t m, int k) {
     uint32_t w = static_cast<uint32_t>(m);
@@ -451,6 +469,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
             const int qrow = q0 + row;
             float M = -INFINITY;  // running max of raw scores
             int C = 0;            // running count of keys equal to M (only C > 1 kept outside statistics)
+            bool tied = false;    // statistics variant: C > 1 as the timed variant decides it
             float m = -INFINITY;  // current shift, raw units
             float mc = -INFINITY; // m * sl2
             float l = 0.f;
@@ -501,26 +520,14 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                     // Only C > 1 matters here.  A tile max equal to the running
                     // max adds at least one tie to the C >= 1 already counted, so
                     // C > 1 follows without a count; only a new running max needs
-                    // to know whether the tile holds it twice.  Two distinct keys
-                    // differ either in c mod 8 or, if not, in c div 8; so the
-                    // tile max occurs at least twice exactly when at least two of
-                    // the mod-8 chain maxima, or two of the maxima of the 16
-                    // blocks of 8 consecutive keys, equal it.
+                    // to know whether the tile holds it twice.
                     const bool newmax = tm > M;
                     const bool same = tm == M;
                     if (__any_sync(0xffffffffu, newmax)) {
-                        int na = 0, nb = 0;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) na += (mx[e] == tm) ? 1 : 0;
-#pragma unroll
-                        for (int b = 0; b < kBlockN / 8; ++b) {
-                            const float* v8 = &s[8 * b];
-                            const float bm = fmax3(fmax3(v8[0], v8[1], v8[2]), fmax3(v8[3], v8[4], v8[5]), fmaxf(v8[6], v8[7]));
-                            nb += (bm == tm) ? 1 : 0;
-                        }
+                        const bool rep2 = tile_max_repeats(s, mx, tm);
                         if (newmax) {
                             M = tm;
-                            C = (na >= 2 || nb >= 2) ? 2 : 1;
+                            C = rep2 ? 2 : 1;
                         }
                     }
                     if (same) C = 2;
@@ -537,10 +544,15 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                             for (int e = 0; e < 8; ++e) tcs[e] += (s[c + e] == tm) ? 1 : 0;
                         tc = ((tcs[0] + tcs[1]) + (tcs[2] + tcs[3])) + ((tcs[4] + tcs[5]) + (tcs[6] + tcs[7]));
                     }
+                    // the shift follows the same decision as in the timed
+                    // variant (tile_max_repeats), so that the unit-probability
+                    // counts reported here check it against the exact count
                     if (tm > M) {
                         M = tm;
                         C = tc;
+                        tied = tile_max_repeats(s, mx, tm);
                     } else if (tm == M) {
+                        tied = true;
                         C += tc;
                     }
                 } else {
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(FwdLayout<D, MODE, NQ>::kThreads, 1)
                 float m_new = M;
                 if (MODE == 1 && p.shift) {
                     m_new = m_fix;
-                } else if (MODE == 1 && C > 1) {
+                } else if (MODE == 1 && (STATS ? tied : C > 1)) {
                     if (M > 0.f) m_new = p.beta * M;
                     else if (M < 0.f) m_new = 0.f;
                 }

@@ -130,10 +130,9 @@ def test_stabilised_tie_decisions_agree_across_score_magnitudes(fa):
     # Ternary Q, K times 2^a give integer scores times 2^(2a), and the scale
     # 2^(-2a)/4 maps all three to the same logits.  Every FP32 product in the
     # kernel then differs only by an exact power of two, so the outputs are
-    # bit-identical exactly when the tie decisions agree.  Row maxima near
-    # 1 (a = 0) take the saturated-FMA count; those below 2^-76 (a = -42) or
-    # above 2^27 (a = 14) take the compare loop.  Each is also checked
-    # against the oracle, and mode 1 must differ from mode 0.
+    # bit-identical exactly when the tie decisions agree, for row maxima
+    # near 1 (a = 0), below 2^-76 (a = -42) and above 2^27 (a = 14).  Each is
+    # also checked against the oracle, and mode 1 must differ from mode 0.
     from types import SimpleNamespace
     from precision_flash_attention_attn_gb300.inputs import bf16_bits
     rng = np.random.default_rng(31)
