@@ -250,16 +250,14 @@ int fa_bwd_heads(const void* q, const void* k, const void* v, const void* o_bf16
  * 30 MiB part that holds fa_bwd's Z bytes (see fa_bwd) and a 2 MiB part that
  * holds its R bytes; problems whose Z or R does not fit (at d = 64, B*H*N
  * above about 122,000 rows) are rejected with FA_ERR_INVALID_ARG before
- * anything is enqueued (fa_last_error says why).  Each call leaves the 30 MiB
- * part at zero again, so no clearing is enqueued.  The first call on a device also looks up the
+ * anything is enqueued (fa_last_error says why).  As in fa_bwd, the first
+ * kernel clears the accumulator.  The first call on a device also looks up the
  * array's device address on that device; make that first call before any
  * stream capture (a first call made while `stream` is capturing is refused
- * with FA_ERR_INVALID_ARG).  All calls share the one array and it keeps the
- * previous call's contents (a call that timed out may leave the 30 MiB part
- * dirty: fa_device_status with reset clears it), so calls whose execution
- * overlaps on the GPU -- e.g. on two streams without an ordering between them
- * -- race on the scratch and give wrong results: serialise them.  Allocates
- * nothing and calls no allocating routine.
+ * with FA_ERR_INVALID_ARG).  All calls share the one array, so calls whose
+ * execution overlaps on the GPU -- e.g. on two streams without an ordering
+ * between them -- race on the scratch and give wrong results: serialise
+ * them.  Allocates nothing and calls no allocating routine.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -342,8 +340,7 @@ int fa_delta_error_split(const void* q, const void* k, const void* v, const void
  * row whose LSE is not finite (every Pbar of the row underflowed, e.g. a large
  * beta on a large repeated maximum; its O is then not finite either),
  * FA_ERR_CUDA if the synchronisation failed, else FA_OK.  reset != 0 clears
- * the recorded status (and, after a timeout, the allocation-free backward's
- * accumulator).
+ * the recorded status.
  */
 int fa_device_status(fa_stream_t stream, int reset);
 

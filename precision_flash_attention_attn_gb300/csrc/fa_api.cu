@@ -244,13 +244,12 @@ bool bwd_pointers_ok(const void* q, const void* k, const void* v, const void* o,
 }
 
 // Enqueue the backward kernels.  `zero` is the zero region (bwd_sizes
-// layout), `rows` the row region.  clean = 1: the zero region is already zero
-// and is to be left at zero again (the allocation-free scratch); clean = 0:
-// a fresh workspace, which the pre kernel clears.  Arguments are already
-// validated.
+// layout), which the first kernel clears right before the main kernel adds
+// into it (its lines are then still in L2), `rows` the row region.
+// Arguments are already validated.
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                     void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale, int mode,
-                    const DeviceInfo* di, void* zero, void* rows, int clean, cudaStream_t st, int delta_given = 0,
+                    const DeviceInfo* di, void* zero, void* rows, cudaStream_t st, int delta_given = 0,
                     const float* o32 = nullptr, uint64_t fp32_mask = 0, int layout = FA_LAYOUT_BHND) {
     const int BH = B * H;
     const fa::RowLayout lay = layout_of(layout, H, N, d);
@@ -282,8 +281,7 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
     a.dq_acc = dq_acc;
     a.lse2 = lse2;
     a.delta = delta;
-    a.zero_acc = clean ? 0 : 1;  // a fresh workspace is cleared by the pre kernel
-    a.clean = clean;
+    a.zero_acc = 1;
     a.delta_given = delta_given;
     a.o32 = o32;
     a.fp32_mask = fp32_mask;
@@ -522,7 +520,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
     }
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
-                             static_cast<char*>(ws) + z.zero_bytes(), 0, st);
+                             static_cast<char*>(ws) + z.zero_bytes(), st);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;
@@ -552,7 +550,7 @@ int fa_bwd_layout(const void* q, const void* k, const void* v, const void* o, co
     }
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
-                             static_cast<char*>(ws) + z.zero_bytes(), 0, st, 0, nullptr, 0, layout);
+                             static_cast<char*>(ws) + z.zero_bytes(), st, 0, nullptr, 0, layout);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
     return rc;
@@ -589,7 +587,7 @@ int fa_bwd_heads(const void* q, const void* k, const void* v, const void* o_bf16
     const void* o_any = (mask[0] | mask[1]) ? o_bf16 : static_cast<const void*>(o_fp32);
     if (rc == FA_OK)
         rc = launch_backward(q, k, v, o_any, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, 0, di, ws,
-                             static_cast<char*>(ws) + z.zero_bytes(), 0, st, 0, o_fp32,
+                             static_cast<char*>(ws) + z.zero_bytes(), st, 0, o_fp32,
                              mask[2] ? mask[2] : 0);
     const cudaError_t fe = cudaFreeAsync(ws, st);
     if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
@@ -650,7 +648,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
         }
         // o is not read: delta is given; pass a valid pointer for the unused argument
         if (rc == FA_OK)
-            rc = launch_backward(q, k, v, dO, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, 0, di, ws, rows, 0, st, 1);
+            rc = launch_backward(q, k, v, dO, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, 0, di, ws, rows, st, 1);
         const cudaError_t fe = cudaFreeAsync(ws, st);
         if (fe != cudaSuccess && rc == FA_OK) rc = cuda_fail("cudaFreeAsync(workspace)", fe);
         return rc;
@@ -743,12 +741,10 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
     if ((rc = device_info(&di))) return rc;
     void* ws = nullptr;
     if ((rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &ws))) return rc;
-    // The zero region is zero from load time and every completed call leaves
-    // it so (clean = 1); fa_device_status clears it after a timeout.  The row
-    // region sits apart from it, at the end of the array, so that a call with
-    // other sizes never finds row values where it needs zeros.
+    // The zero region (the dQ accumulator) is cleared by the first kernel of
+    // every call; the row region sits at the end of the array.
     return launch_backward(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, mode, di, ws,
-                           static_cast<char*>(ws) + kNoallocZeroBytes, 1, static_cast<cudaStream_t>(stream));
+                           static_cast<char*>(ws) + kNoallocZeroBytes, static_cast<cudaStream_t>(stream));
 }
 
 int fa_tie_stats(const void* q, const void* k, const void* v, const void* o, int B, int H, int N, int d,
@@ -883,14 +879,6 @@ int fa_device_status(fa_stream_t stream, int reset) {
     if (reset && h != 0) {
         const int zero = 0;
         if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
-        // a launch that gave up may have left the allocation-free backward's
-        // zero region (the accumulator) dirty
-        void* scratch = nullptr;
-        {
-            std::lock_guard<std::mutex> lk(g_noalloc_mu);
-            scratch = g_noalloc_addr[di->dev];
-        }
-        if (scratch && cudaMemset(scratch, 0, kNoallocZeroBytes) != cudaSuccess) return FA_ERR_CUDA;
     }
     if (h & 1) return FA_ERR_TIMEOUT;
     return h == 0 ? FA_OK : FA_ERR_NONFINITE;

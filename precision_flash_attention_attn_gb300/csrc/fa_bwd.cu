@@ -53,9 +53,8 @@ struct BwdParams {
     void* dq;             // [BH, N, d] BF16 output
     float* lse2;          // [BH, Npad]: -LSE*log2(e), -inf on padded rows
     float* delta;         // [BH, Npad]: -alpha*rowsum(dO o O), 0 on padded rows
-    int clean;            // 1: leave the accumulator and the barrier words at zero afterwards
     int delta_given;      // 1: delta already holds -alpha*rowsum(dP o P); pre forms lse2 only
-    int zero_acc;         // 1: pre also clears the dQ accumulator (a fresh workspace)
+    int zero_acc;         // 1: pre also clears the dQ accumulator
     const float* o32;     // per-head modes: FP32 O of the heads in fp32_mask (o holds the others)
     uint64_t fp32_mask;
     int H;
@@ -187,14 +186,13 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdParams p,
 
 // -------------------------------------------------------------- convert ----
 // dQ accumulator (FP32) -> BF16 in the caller's layout, eight elements per
-// thread and step, four steps' loads in flight; with `clean` the accumulator
-// is zeroed as it is read.
+// thread and step, four steps' loads in flight.
 template <int D>
 __global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const BwdParams p) {
     constexpr int kChunks = D / 8;  // eight-element chunks per row
     griddep_launch_dependents();
     griddep_wait();  // every reduce-add of the main kernel has landed
-    float4* acc = reinterpret_cast<float4*>(p.dq_acc);
+    const float4* acc = reinterpret_cast<const float4*>(p.dq_acc);
     uint4* dq = reinterpret_cast<uint4*>(p.dq);
     // BH * Npad * d < 2^31 (checked on the host): 32-bit chunk indices
     const int n8 = p.BH * p.N * kChunks;
@@ -227,10 +225,6 @@ __global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const BwdParams
                     dst = (p.lay.row(bh, row - bh * p.N) >> 3) + static_cast<size_t>(e - row * kChunks);
                 }
                 dq[dst] = w;
-                if (p.clean) {
-                    acc[2 * static_cast<size_t>(e)] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    acc[2 * static_cast<size_t>(e) + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
             }
         }
     }
@@ -861,7 +855,6 @@ BwdParams make_params(const BwdArgs& a) {
     p.dq = a.dq;
     p.lse2 = a.lse2;
     p.delta = a.delta;
-    p.clean = a.clean;
     p.delta_given = a.delta_given;
     p.zero_acc = a.zero_acc;
     p.o32 = a.o32;

@@ -96,8 +96,7 @@ struct BwdArgs {
     float* dq_acc;                // FP32 [BH, N, d] workspace
     float* lse2;                  // FP32 [BH, Npad] workspace: LSE * log2(e)
     float* delta;                 // FP32 [BH, Npad] workspace: rowsum(dO o O)
-    int zero_acc;                 // 1: the pre kernel clears dq_acc (a fresh workspace)
-    int clean;                    // 1: leave dq_acc at zero when done
+    int zero_acc;                 // 1: the pre kernel clears dq_acc
     int delta_given;              // 1: delta is already in place (rowsum(dP o P) pre-pass)
     const float* o32 = nullptr;   // per-head modes: FP32 O of the heads in fp32_mask
     uint64_t fp32_mask = 0;       // heads h (bit h) whose delta uses o32 instead of o
