@@ -442,6 +442,32 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = world * flop_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
 
+    # The same copies alone, back to back on the stream (best of 3).  A step
+    # cannot end before its inputs are in, its first mode has run and every
+    # output is out, so these give the end-to-end number's own bound.
+    def copies_ms(issue):
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            issue()
+            b.record(stream)
+            b.synchronize()
+            best = a.elapsed_time(b) if best is None else min(best, a.elapsed_time(b))
+        return best
+
+    def issue_h2d():
+        for n in pin:
+            dq_in[n].view(torch.int16).copy_(pin[n], non_blocking=True)
+
+    def issue_d2h():
+        for _, m in MODES:
+            for kname, t in outs[m].items():
+                host_out[m][kname].copy_(t, non_blocking=True)
+
+    h2d_ms, d2h_ms = copies_ms(issue_h2d), copies_ms(issue_d2h)
+    e2e_bound_ms = h2d_ms + per_mode_ms[0] / args.steps + d2h_ms
+
     # ------------------------------------------- fa_bwd against fa_bwd_noalloc --
     # The same backward through both entry points, called eagerly one by one
     # (fa_bwd allocates its workspace from the stream's pool, clears its
@@ -512,7 +538,13 @@ def run_ours(args):
         "kernels": kernel_share,
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                "copy_bound": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
+                               "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+                               "bound_ms_per_step": e2e_bound_ms,
+                               "frac": e2e_bound_ms / (e2e_ms / e2e_steps),
+                               "how": "inputs in, then the first mode, then every output out, each timed "
+                                      "alone (copies best of 3, pinned host memory)"}},
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
