@@ -67,8 +67,8 @@ def test_withheld_tile_times_out_and_the_context_survives(fa, monkeypatch):
 
 
 def test_backward_after_a_timeout_is_correct(fa, monkeypatch):
-    # the backward's grid barriers and scratch are unaffected by a forward
-    # that timed out
+    # the backward (its three launches and its scratch) is unaffected by a
+    # forward that timed out
     import torch
     from gpu_helpers import GRAD_REL_TOL, rel_fro
     c = case("tiny")
