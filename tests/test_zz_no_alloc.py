@@ -54,3 +54,28 @@ def test_noalloc_backward_matches_fa_bwd_twice_in_a_row(B, H, N, d, causal):
             for name, g, r in zip(("dq", "dk", "dv"), got, ref):
                 err = rel_fro(host_f64(g), r, floor)
                 assert err <= GRAD_REL_TOL, (name, mode, _call, err)
+
+
+@pytest.mark.gpu
+def test_noalloc_is_fa_bwd_at_the_gpt2_small_size():
+    """The timed path at its full size: fa_bwd_noalloc runs the same kernels as
+    fa_bwd (whose gradients the backward tests check against the oracle for
+    every head at this size), so dK and dV are bit-identical and dQ differs
+    only by the order of the FP32 reduce-adds into its accumulator."""
+    import torch
+    from conftest import case
+    fa = _fa()
+    c = case("gpt2s")
+    B, H, N, d = c.B, c.H, c.N, c.d
+    q, k, v, do = (dev_bf16(getattr(c, n)) for n in ("q", "k", "v", "do"))
+    for mode in (0, 1, 2):
+        o, lse = fa.attention_fwd(q, k, v, c.causal, c.scale, mode)
+        ref = fa.attention_bwd(q, k, v, o, lse, do, c.causal, c.scale, mode)
+        for _call in range(2):
+            got = [torch.full_like(q, float("nan")) for _ in range(3)]
+            fa.fa_bwd_noalloc(q, k, v, o, lse, do, *got, B, H, N, d, c.causal, c.scale, mode)
+            torch.cuda.synchronize()
+            assert fa.fa_device_status() == 0
+            assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), (mode, _call)
+            err = rel_fro(host_f64(got[0]), host_f64(ref[0]))
+            assert err <= 1e-4, (mode, _call, err)
