@@ -396,6 +396,24 @@ def run_ours(args):
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel timeout during the timed region")
 
+    # The timed launches computed what the same calls compute eagerly (the
+    # calls the parity tests check): O, LSE, dK and dV bit for bit, dQ up to
+    # the order of the FP32 reduce-adds into its accumulator.
+    same_as_eager = True
+    for _, m in MODES:
+        got = outs[m]
+        ref = {kname: torch.empty_like(t) for kname, t in got.items()}
+        fa.fa_fwd(q, k, v, ref["o"], ref["lse"], B, H, N, d, causal, scale, m, stream)
+        bwd_timed(q, k, v, ref["o"], ref["lse"], do, ref["dq"], ref["dk"], ref["dv"], B, H, N, d, causal, scale,
+                  m, stream)
+        torch.cuda.synchronize()
+        exact = all(torch.equal(got[kname], ref[kname]) for kname in ("o", "lse", "dk", "dv"))
+        dq_rel = float((got["dq"].float() - ref["dq"].float()).norm() / ref["dq"].float().norm())
+        if not exact or not dq_rel <= 1e-4:
+            same_as_eager = False
+    if not same_as_eager:
+        raise RuntimeError("the timed launches' outputs differ from the same calls made eagerly")
+
     per_mode_ms = [0.0] * len(MODES)
     for e in ev:
         for i in range(len(MODES)):
@@ -537,6 +555,7 @@ def run_ours(args):
         "roofline": roof,
         "kernels": kernel_share,
         "gpu_launches": gpu_launches,
+        "outputs_match_eager_calls": same_as_eager,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
                 "copy_bound": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
