@@ -37,7 +37,13 @@
 //            back, leaving the accumulator ready for the next call).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <climits>
 #include <cstdio>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -298,11 +304,29 @@ struct BwdLayout {
 };
 
 // Work items are (key tile, batch-head) pairs numbered longest first (causal:
-// key tile 0 sees every query tile).  CTA c takes items in a snake order over
-// rounds of gridDim.x, as the forward does.
-__device__ __forceinline__ int bwd_item(int r) {
-    const int G = static_cast<int>(gridDim.x);
+// key tile 0 sees every query tile).  The host assigns them to the CTAs by
+// longest-processing-time-first list scheduling: each item in turn, longest
+// first, goes to the CTA with the fewest query tiles so far (at the GPT-2
+// small shape the busiest SM gets 23 tiles, a snake order over rounds of the
+// grid gives it 24).  items[start[c] .. start[c + 1]) are CTA c's items in
+// the order it runs them.  n = 0 (more items or CTAs than the table holds):
+// snake order.
+constexpr int kSchedMaxCta = 160;
+constexpr int kSchedMaxItems = 4096;
+struct BwdSched {
+    int n;
+    uint16_t start[kSchedMaxCta + 1];
+    uint16_t items[kSchedMaxItems];
+};
+
+// The item CTA blockIdx.x runs in its round r, or INT_MAX past its last.
+__device__ __forceinline__ int bwd_item(const BwdSched& sc, int r) {
     const int c = static_cast<int>(blockIdx.x);
+    if (sc.n > 0) {
+        const int b = sc.start[c], e = sc.start[c + 1];
+        return r < e - b ? static_cast<int>(sc.items[b + r]) : INT_MAX;
+    }
+    const int G = static_cast<int>(gridDim.x);
     return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
@@ -311,7 +335,8 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
-               const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dv, const BwdParams p,
+               const __grid_constant__ BwdSched sched) {
     using L = BwdLayout<D>;
     constexpr int QS = L::kQStages;
     constexpr int KVB = L::kKVBufs;
@@ -388,7 +413,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             int g = 0;  // query tiles loaded so far (all items)
             int n = 0;  // items started
             for (int r = 0; ok; ++r, ++n) {
-                const int itm = bwd_item(r);
+                const int itm = bwd_item(sched, r);
                 if (itm >= p.n_items) break;
                 const int bh = item_bh(itm), kt = item_kt(itm);
                 const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
@@ -491,7 +516,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         // for this tile's dQ to be drained, after the dQ product, and a new
         // item starts only after the previous one's products.
         int g = 0;  // query tiles processed so far (all items)
-        int itm = bwd_item(0);
+        int itm = bwd_item(sched, 0);
         bool head_issued = false;  // this item's first S^T/dP^T already issued
         for (int r = 0, n = 0; ok && itm < p.n_items; ++r, ++n) {
             const int kt = item_kt(itm);
@@ -499,7 +524,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
             const int kb = n % KVB;
             const uint32_t sK = sb + L::kK + kb * L::kTile;
             const uint32_t sV = sb + L::kV + kb * L::kTile;
-            const int itm_next = bwd_item(r + 1);
+            const int itm_next = bwd_item(sched, r + 1);
             const bool has_next = itm_next < p.n_items;
             const uint32_t sK_next = sb + L::kK + ((n + 1) % KVB) * L::kTile;
             const uint32_t sV_next = sb + L::kV + ((n + 1) % KVB) * L::kTile;
@@ -611,7 +636,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         bool ok = true;
         int g = 0;  // query tiles so far (all items)
         for (int r = 0, n = 0; ok; ++r, ++n) {
-            const int itm = bwd_item(r);
+            const int itm = bwd_item(sched, r);
             if (itm >= p.n_items) break;
             const int bh = item_bh(itm), kt = item_kt(itm);
             const int hh = bh % p.H, bb = bh / p.H;  // head and batch of the tile coordinates
@@ -711,7 +736,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
         int g = 0;  // query tiles processed so far (all items)
 
         for (int r = 0; ok; ++r) {
-            const int itm = bwd_item(r);
+            const int itm = bwd_item(sched, r);
             if (itm >= p.n_items) break;
             const int kt = item_kt(itm);
             const int qt_begin = item_qt0(kt);
@@ -914,6 +939,39 @@ cudaError_t launch_pre(const BwdParams& p, int num_sms, cudaStream_t stream) {
     return e;
 }
 
+// The item schedule of a launch (see BwdSched), kept for the last shape this
+// host thread launched.  Items are numbered longest first, so list scheduling
+// takes them in index order.
+const BwdSched& item_schedule(int n_items, int BH, int n_qt, bool causal, int n_cta) {
+    thread_local BwdSched sc;
+    thread_local int key[5] = {-1, -1, -1, -1, -1};
+    const int k[5] = {n_items, BH, n_qt, causal ? 1 : 0, n_cta};
+    if (std::equal(k, k + 5, key)) return sc;
+    std::copy(k, k + 5, key);
+    sc.n = 0;
+    if (n_items > kSchedMaxItems || n_cta > kSchedMaxCta || n_cta < 1) return sc;
+    std::vector<std::vector<int>> per(static_cast<size_t>(n_cta));
+    using Slot = std::pair<long long, int>;  // (query tiles so far, CTA)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> least;
+    for (int c = 0; c < n_cta; ++c) least.push({0, c});
+    for (int it = 0; it < n_items; ++it) {
+        const int kt = it / BH;
+        const int tiles = causal ? n_qt - kt : n_qt;
+        const Slot s0 = least.top();
+        least.pop();
+        per[static_cast<size_t>(s0.second)].push_back(it);
+        least.push({s0.first + tiles, s0.second});
+    }
+    int pos = 0;
+    for (int c = 0; c < n_cta; ++c) {
+        sc.start[c] = static_cast<uint16_t>(pos);
+        for (int it : per[static_cast<size_t>(c)]) sc.items[pos++] = static_cast<uint16_t>(it);
+    }
+    sc.start[n_cta] = static_cast<uint16_t>(pos);
+    sc.n = pos;
+    return sc;
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_main(const BwdArgs& a, const BwdParams& p, cudaStream_t stream) {
     using L = BwdLayout<D>;
@@ -927,8 +985,9 @@ cudaError_t launch_main(const BwdArgs& a, const BwdParams& p, cudaStream_t strea
     // persistent: one CTA per SM (or per item, if fewer)
     const int n_cta = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     prof_begin(3, stream);
+    const BwdSched& sched = item_schedule(p.n_items, p.BH, (p.N + kBlockM - 1) / kBlockM, CAUSAL, n_cta);
     e = launch_pdl(kern, dim3(static_cast<unsigned>(n_cta > 0 ? n_cta : 1)), L::kThreads, L::kAlloc, stream,
-                   *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p);
+                   *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dqacc, *a.tm_dk, *a.tm_dv, p, sched);
     prof_end(3, stream);
     if (e != cudaSuccess) {
         cudaFuncAttributes fa_attr{};
