@@ -306,11 +306,11 @@ struct BwdLayout {
 // Work items are (key tile, batch-head) pairs numbered longest first (causal:
 // key tile 0 sees every query tile).  The host assigns them to the CTAs by
 // longest-processing-time-first list scheduling: each item in turn, longest
-// first, goes to the CTA with the fewest query tiles so far (at the GPT-2
-// small shape the busiest SM gets 23 tiles, a snake order over rounds of the
-// grid gives it 24).  items[start[c] .. start[c + 1]) are CTA c's items in
-// the order it runs them.  n = 0 (more items or CTAs than the table holds):
-// snake order.
+// first, goes to the CTA with the fewest query tiles so far.  For 96 causal
+// heads of 8 key tiles on 152 SMs the busiest SM then gets 23 query tiles; a
+// snake order over rounds of the grid gives it 24.  items[start[c] ..
+// start[c + 1]) are CTA c's items in the order it runs them.  n = 0 (more
+// items or CTAs than the table holds): snake order.
 constexpr int kSchedMaxCta = 160;
 constexpr int kSchedMaxItems = 4096;
 struct BwdSched {
