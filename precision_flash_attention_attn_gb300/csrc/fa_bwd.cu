@@ -585,6 +585,11 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                         const uint64_t b = sdesc_sw128(sQ + kk * 2048, 16384, 1024);
                         mma_bf16_ss(tmem + L::kColDK, a, b, kIdAcc, (it > 0 || kk > 0) ? 1u : 0u);
                     }
+                    // d = 128 (a single Q/dO stage, so the next tile's load
+                    // waits for this release): the stage's last readers (S^T,
+                    // dP^T, dV, dK) are issued, so release it before the dQ
+                    // product, which reads only dS^T and K
+                    if (L::kQStages == 1) mma_commit(bar(L::kQEmpty + s));
                 }
                 __syncwarp();
                 // dQ_t = dS K  (A = dS^T buffer read M-major, B = K read N-major)
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(BwdLayout<D>::kThreads, 1)
                         mma_bf16_ss(tmem + L::kColDQ, a, b, kIdDQ, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(L::kDQFull));
-                    mma_commit(bar(L::kQEmpty + s));
+                    if (L::kQStages > 1) mma_commit(bar(L::kQEmpty + s));
                     mma_commit(bar(L::kPDSFree));
                     if (last) {
                         mma_commit(bar(L::kKVEmpty + kb));  // last read of this item's K and V
